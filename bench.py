@@ -1,0 +1,552 @@
+#!/usr/bin/env python
+"""MuonClip step benchmark: prints ONE JSON line.
+
+A step is one pass of the whole hot path on one batch of synthetic input:
+max-logit scan (projections + QK^T max), Muon (momentum, 5 quintic
+Newton-Schulz iterations, RMS matching, weight decay) and QK-Clip, through
+the library's C ABI.  Default workload: an MHA layer in bf16, x [8, 1024,
+1024], 16 heads of 64, tau = 100, Muon on the 1024 x 1024 fp32 masters of
+W_q and W_k.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload c2|c3|c4|c5]
+
+value     = algorithmic TFLOP/s of the step (scan + Newton-Schulz flops per
+            step / device time per step, inputs resident, L2 flushed between
+            timed steps);
+e2e       = the same through the public API with the step's inputs copied
+            host->device from pinned memory and the results read back;
+roofline  = the dominant kernel's algorithmic work per launch / its
+            event-timed duration against the measured peak;
+cpu_baseline = the fp64 oracle on this host's cores on a bounded sample.
+--impl reference times that oracle (the only reference this method has).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import mc_inputs  # noqa: E402
+
+METRIC = "max-logit scan & Newton-Schulz TFLOP/s (% bf16 peak); MuonClip step ms"
+L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work
+# ---------------------------------------------------------------------------
+
+def ns_flops_per_iter(m: int, n: int) -> dict:
+    """Per quintic iteration on an m x n (m <= n) matrix, counting the
+    symmetric products once: Gram m(m+1)n, A A m^2(m+1), B X 2 m^2 n."""
+    return {"gram": m * (m + 1) * n, "poly": m * m * (m + 1), "apply": 2 * m * m * n}
+
+
+def scan_pairs(B, T, causal):
+    return B * (T * (T + 1) // 2 if causal else T * T)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p["bf16_tflops"], p.get("bf16_tflops_sustained"), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+
+class Workload:
+    name = ""
+    desc = ""
+
+    def make(self, device):
+        raise NotImplementedError
+
+    def step(self, s, api):
+        raise NotImplementedError
+
+
+class MhaLayer(Workload):
+    """c2: MHA layer + Muon on the W_q / W_k masters + clip."""
+
+    def __init__(self, B=8, T=1024, D=1024, H=16, dh=64):
+        self.B, self.T, self.D, self.H, self.dh = B, T, D, H, dh
+        self.name = "c2"
+        self.desc = (f"MHA layer bf16 x[{B},{T},{D}] H={H} dh={dh} tau=100 non-causal; "
+                     f"Muon (5 NS steps, mu 0.95, lr 2e-4, wd 0.1, rms 0.2) on fp32 W_q, W_k "
+                     f"[{D},{H * dh}]; QK-Clip of both")
+        N = H * dh
+        m, n = min(D, N), max(D, N)
+        ns = ns_flops_per_iter(m, n)
+        self.units = {
+            "gemm:proj": ("tensor", 2 * 2 * B * T * D * N),
+            "scan": ("tensor", 2 * scan_pairs(B, T, False) * H * dh),
+            "gemm:ns_gram": ("tensor", 2 * ns["gram"]),
+            "gemm:ns_poly": ("tensor", 2 * ns["poly"]),
+            "gemm:ns_apply": ("tensor", 2 * ns["apply"]),
+            "muon_momentum": ("hbm", 2 * D * N * 14),
+            "muon_update": ("hbm", 2 * D * N * 10),
+        }
+        self.scan_flops = self.units["gemm:proj"][1] + self.units["scan"][1]
+        self.ns_flops = 5 * sum(self.units[k][1] for k in ("gemm:ns_gram", "gemm:ns_poly",
+                                                          "gemm:ns_apply"))
+
+    def make(self, device):
+        inp = mc_inputs.c2(device=device, B=self.B, T=self.T, D=self.D, H=self.H, dh=self.dh)
+        import torch
+        s = dict(inp)
+        s["masters"] = [t.clone() for t in inp["w_master"]]
+        s["moms"] = [t.clone() for t in inp["m_prev"]]
+        s["s_max"] = torch.empty(self.H, dtype=torch.float32, device=device)
+        s["gamma"] = torch.empty(self.H, dtype=torch.float32, device=device)
+        return s
+
+    def inputs(self, s):
+        """Per-step inputs a trainer would hand over: activations, grads."""
+        return [s["x"]] + s["grad"]
+
+    def outputs(self, s):
+        return [s["s_max"], s["gamma"]]
+
+    def step(self, s, api, marks=None):
+        api.mc_max_logits_mha(s["x"], s["wq"], s["wk"], self.H, self.dh, s_max=s["s_max"])
+        if marks:
+            marks[0].record()
+        api.mc_muon_step(s["masters"], s["grad"], s["moms"], lr=mc_inputs.LR, mu=mc_inputs.MU,
+                         wd=mc_inputs.WD, rms=mc_inputs.RMS, steps=mc_inputs.NS_STEPS)
+        if marks:
+            marks[1].record()
+        api.mc_qk_clip_mha(s["masters"][0], s["masters"][1], self.H, self.dh, s["s_max"],
+                           s["tau"], gamma=s["gamma"])
+
+    # --- oracle sample for the CPU baseline ---------------------------------
+    def oracle_sample(self, s):
+        import oracle
+        x = s["x"][:1].cpu()
+        wq, wk = s["wq"].cpu(), s["wk"].cpu()
+        w0, g0, m0 = (t[0].cpu() for t in (s["w_master"], s["grad"], s["m_prev"]))
+        heads = [0, 1]
+        t0 = time.perf_counter()
+        oracle.max_logits_mha(x, wq, wk, self.H, self.dh, False, heads=heads)
+        oracle.muon_step(w0, g0, m0, lr=mc_inputs.LR)
+        dt = time.perf_counter() - t0
+        N = self.H * self.dh
+        m, n = min(self.D, N), max(self.D, N)
+        flops = len(heads) * (2 * 2 * self.T * self.D * self.dh + 2 * self.T * self.T * self.dh)
+        flops += 5 * sum(2 * v for v in ns_flops_per_iter(m, n).values())
+        return flops, dt, (f"2 of {self.B * self.H} (sequence, head) scans and 1 of 2 "
+                           f"Muon steps ({self.D}x{N}), fp64")
+
+
+class ExpertBatch(Workload):
+    """c4: Muon on 48 up + 48 down expert matrices (no scan)."""
+
+    def __init__(self, n_up=48, n_down=48):
+        self.n_up, self.n_down = n_up, n_down
+        self.name = "c4"
+        self.desc = (f"Muon batch: {n_up} x 7168x2048 + {n_down} x 2048x7168 fp32, 5 NS steps "
+                     "(bf16 operands, fp32 accumulation)")
+        ns = ns_flops_per_iter(2048, 7168)
+        cnt = n_up + n_down
+        self.units = {
+            "gemm:ns_gram": ("tensor", 2 * ns["gram"] * cnt),
+            "gemm:ns_poly": ("tensor", 2 * ns["poly"] * cnt),
+            "gemm:ns_apply": ("tensor", 2 * ns["apply"] * cnt),
+            "muon_momentum": ("hbm", cnt * 2048 * 7168 * 14),
+            "muon_update": ("hbm", cnt * 2048 * 7168 * 10),
+        }
+        self.scan_flops = 0
+        self.ns_flops = 5 * (self.units["gemm:ns_gram"][1] + self.units["gemm:ns_poly"][1]
+                             + self.units["gemm:ns_apply"][1])
+
+    def make(self, device):
+        return mc_inputs.c4(device=device, n_up=self.n_up, n_down=self.n_down)
+
+    def inputs(self, s):
+        return s["grad"]
+
+    def outputs(self, s):
+        return []
+
+    def step(self, s, api, marks=None):
+        if marks:
+            marks[0].record()
+        api.mc_muon_step(s["w"], s["grad"], s["m_prev"], lr=mc_inputs.LR)
+        if marks:
+            marks[1].record()
+
+    def oracle_sample(self, s):
+        import oracle
+        t0 = time.perf_counter()
+        oracle.newton_schulz(s["m_prev"][0][:512].cpu(), 5)
+        dt = time.perf_counter() - t0
+        m, n = 512, 2048
+        flops = 5 * sum(2 * v for v in ns_flops_per_iter(m, n).values())
+        return flops, dt, "Newton-Schulz of one 512x2048 slice of an expert momentum, fp64"
+
+
+class MlaLayer(Workload):
+    """c3 / c5: MLA layer scan (+ Muon on its 4 projections for c5) + clip."""
+
+    def __init__(self, which="c5", B=None, T=None):
+        self.which = which
+        self.name = which
+        self.B = B if B is not None else (1 if which == "c5" else 16)
+        self.T = T if T is not None else (32768 if which == "c5" else 4096)
+        self.muon = which == "c5"
+        self.desc = (f"K2-shaped MLA layer bf16 x[{self.B},{self.T},7168] H=64 q_lora 1536 "
+                     f"kv_lora 512 nope 128 rope 64 causal"
+                     + ("; Muon on W_qa, W_qb, W_kva, W_kb; MLA clip" if self.muon else ""))
+        BT = self.B * self.T
+        proj = 2 * BT * (7168 * 1536 + 7168 * 576 + 1536 * 64 * 192 + 512 * 64 * 128)
+        self.units = {"gemm:proj": ("tensor", proj / 2),  # two launches per step
+                      "scan": ("tensor", 2 * scan_pairs(self.B, self.T, True) * 64 * 192)}
+        self.scan_flops = proj + self.units["scan"][1]
+        self.ns_flops = 0
+        if self.muon:
+            for r, c in [(7168, 1536), (1536, 12288), (7168, 576), (512, 8192)]:
+                m, n = min(r, c), max(r, c)
+                self.ns_flops += 5 * sum(2 * v for v in ns_flops_per_iter(m, n).values())
+
+    def make(self, device):
+        fn = mc_inputs.c5 if self.which == "c5" else mc_inputs.c3
+        inp = fn(device=device, B=self.B, T=self.T)
+        import torch
+        s = dict(inp)
+        if self.muon:
+            s["masters"] = [t.clone() for t in inp["w_master"]]
+            s["moms"] = [t.clone() for t in inp["m_prev"]]
+        s["s_max"] = torch.empty(64, dtype=torch.float32, device=device)
+        s["gamma"] = torch.empty(64, dtype=torch.float32, device=device)
+        return s
+
+    def inputs(self, s):
+        return [s["x"]] + (s["grad"] if self.muon else [])
+
+    def outputs(self, s):
+        return [s["s_max"], s["gamma"]]
+
+    def step(self, s, api, marks=None):
+        api.mc_max_logits_mla(s["x"], s["w_qa"], s["w_qb"], s["w_kva"], s["w_kb"], 64, 128, 64,
+                              s["rope_base"], causal=True, s_max=s["s_max"])
+        if marks:
+            marks[0].record()
+        if self.muon:
+            api.mc_muon_step(s["masters"], s["grad"], s["moms"], lr=mc_inputs.LR)
+        if marks:
+            marks[1].record()
+        if self.muon:
+            api.mc_qk_clip_mla(s["masters"][1], s["masters"][3], 64, 128, 64, s["s_max"], s["tau"],
+                               gamma=s["gamma"])
+        else:
+            api.mc_qk_clip_mla(s["w_qb"], s["w_kb"], 64, 128, 64, s["s_max"], s["tau"],
+                               gamma=s["gamma"])
+
+    def oracle_sample(self, s):
+        import oracle
+        T = min(self.T, 512)
+        t0 = time.perf_counter()
+        oracle.max_logits_mla(s["x"][:1, :T].cpu(), s["w_qa"].cpu(), s["w_qb"].cpu(),
+                              s["w_kva"].cpu(), s["w_kb"].cpu(), 64, 128, 64, s["rope_base"],
+                              True, heads=[0])
+        dt = time.perf_counter() - t0
+        flops = 2 * T * (7168 * 1536 + 7168 * 576) + 2 * T * (1536 * 192 + 512 * 128)
+        flops += 2 * (T * (T + 1) // 2) * 192
+        return flops, dt, f"one head of the MLA scan over the first {T} tokens, fp64"
+
+
+WORKLOADS = {"c2": lambda: MhaLayer(), "c4": lambda: ExpertBatch(), "c3": lambda: MlaLayer("c3"),
+             "c5": lambda: MlaLayer("c5")}
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) >= 9:
+                    rows.append(p)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        busy = [v for v in sm if v > 0.5 * max(sm)] if sm else []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, wl):
+    """The fp64 oracle on the host cores: each step is one bounded sample of
+    the workload (inputs drawn on the CPU)."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    s = wl.make("cpu")
+    for _ in range(min(args.warmup, 1)):
+        wl.oracle_sample(s)
+    times, flops, sample = [], 0, ""
+    for _ in range(args.steps):
+        f, dt, sample = wl.oracle_sample(s)
+        times.append(dt)
+        flops = f
+    tot = sum(times)
+    value = flops * len(times) / tot / 1e12
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot / len(times), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.desc, "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl")
+
+    from muonclip_mc_max_gb300 import api, build
+    build.build()
+    api.load_library()
+    s = wl.make(device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(max(args.warmup, 3)):
+        wl.step(s, api)
+    assert api.mc_read_device_status(clear=True) == 0, "device status set during warm-up"
+
+    # ---- timed region: device time per step, L2 flushed between steps ----
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    launches0 = api.mc_launch_count()
+    for k in range(K):
+        flush.zero_()
+        e0, m0, m1, e1 = ev[k]
+        e0.record(stream)
+        wl.step(s, api, marks=(m0, m1))
+        e1.record(stream)
+    barrier()
+    launches = api.mc_launch_count() - launches0
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, _, _, b in ev]
+    scan_ms = [a.elapsed_time(m) for a, m, _, _ in ev]
+    muon_ms = [m.elapsed_time(n) for _, m, n, _ in ev]
+    tot_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([tot_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot_ms = float(t.item())
+    ms = tot_ms / K
+    flops = wl.scan_flops + wl.ns_flops
+    value = world * flops / (ms * 1e-3) / 1e12
+    hbm_peak, bf16_peak, bf16_sus, peak_src = load_peaks()
+
+    # ---- per-kernel event times (separate pass, same steps) ----
+    api.mc_trace_enable(True)
+    for k in range(K):
+        flush.zero_()
+        wl.step(s, api)
+    torch.cuda.synchronize()
+    api.mc_trace_enable(False)
+    trace = api.mc_trace_collect()
+    kernels = {}
+    for name, (n, tms) in trace.items():
+        entry = {"launches_per_step": n / K, "ms_per_launch": tms / n,
+                 "share": None}
+        if name in wl.units:
+            kind, work = wl.units[name]
+            if kind == "tensor":
+                entry["achieved_tflops"] = work / (tms / n * 1e-3) / 1e12
+            else:
+                entry["achieved_gbs"] = work / (tms / n * 1e-3) / 1e9
+        kernels[name] = entry
+    tot_k = sum(v[1] for v in trace.values()) or 1.0
+    for name, (n, tms) in trace.items():
+        kernels[name]["share"] = tms / tot_k
+    dominant = max((k for k in kernels if k in wl.units), key=lambda k: trace[k][1])
+    kind, work = wl.units[dominant]
+    dur = trace[dominant][1] / trace[dominant][0] * 1e-3
+    if kind == "tensor":
+        achieved = work / dur / 1e12
+        roof = {"kernel": dominant, "bound": "tensor", "achieved": achieved, "peak": bf16_peak,
+                "unit": "TFLOP/s", "frac": achieved / bf16_peak, "traffic": None,
+                "peak_kind": f"{peak_src} bf16 dense (burst)"}
+    else:
+        achieved = work / dur / 1e9
+        roof = {"kernel": dominant, "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
+                "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": None,
+                "peak_kind": f"{peak_src} HBM copy"}
+    assert api.mc_read_device_status(clear=True) == 0, "device status set during timing"
+
+    # ---- end to end through the public API (pinned H2D inputs, D2H results) ----
+    ins = wl.inputs(s)
+    outs = wl.outputs(s)
+    host_in = [t.detach().cpu().pin_memory() for t in ins]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    barrier()
+    t0 = time.perf_counter()
+    for k in range(K):
+        for hd, dv in zip(host_in, ins):
+            dv.copy_(hd, non_blocking=True)
+        wl.step(s, api)
+        for hd, dv in zip(host_out, outs):
+            hd.copy_(dv, non_blocking=True)
+        stream.synchronize()
+    barrier()
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([e2e_s], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e_value = world * flops * K / e2e_s / 1e12
+
+    line = None
+    if rank == 0:
+        # the oracle on this host's cores, repeated for about 10 s of CPU work
+        f_tot, dt_tot, sample, reps = 0, 0.0, "", 0
+        while dt_tot < 10.0 and reps < 50:
+            f, dt, sample = wl.oracle_sample(s)
+            f_tot += f
+            dt_tot += dt
+            reps += 1
+        cpu = {"value": f_tot / dt_tot / 1e12, "unit": "TFLOP/s",
+               "cores": int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)),
+               "kind": "oracle", "sample": f"{sample}; {reps} repetitions, {dt_tot:.1f} s"}
+        scan_t = statistics.mean(scan_ms)
+        muon_t = statistics.mean(muon_ms)
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": wl.desc, "l2": "flushed between timed steps (256 MiB write)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "muonclip_step_ms": ms,
+            "scan_tflops": (wl.scan_flops / (scan_t * 1e-3) / 1e12) if wl.scan_flops else None,
+            "scan_frac_bf16_peak": ((wl.scan_flops / (scan_t * 1e-3) / 1e12) / bf16_peak)
+            if wl.scan_flops else None,
+            "ns_tflops": (wl.ns_flops / (muon_t * 1e-3) / 1e12) if wl.ns_flops else None,
+            "ns_frac_bf16_peak": ((wl.ns_flops / (muon_t * 1e-3) / 1e12) / bf16_peak)
+            if wl.ns_flops else None,
+            "scan_ms": scan_t, "muon_ms": muon_t,
+            "roofline": roof,
+            "kernels": kernels,
+            "gpu_launches": int(launches),
+            "clocks": clk,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c2")
+    args = ap.parse_args()
+    wl = WORKLOADS[args.workload]()
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

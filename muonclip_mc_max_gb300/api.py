@@ -1,0 +1,387 @@
+"""Thin ctypes binding of ``include/mc_max.h``.
+
+Every function carries the C entry point's name and only marshals
+arguments: torch tensors supply device pointers, the caller's current CUDA
+stream is passed through, and workspaces are torch-allocated byte buffers.
+All arithmetic runs in the CUDA library; if ``libmc_max.so`` is missing this
+module raises instead of computing anything elsewhere.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+from .build import library_path
+
+__all__ = [
+    "MCError", "load_library", "header_symbols", "Workspace",
+    "mc_status_string", "mc_read_device_status",
+    "mc_max_logits_mha", "mc_max_logits_mha_workspace_size",
+    "mc_max_logits_mla", "mc_max_logits_mla_workspace_size",
+    "mc_qk_clip_mha", "mc_qk_clip_mla", "mc_qk_clip_global",
+    "mc_newton_schulz", "mc_newton_schulz_workspace_size",
+    "mc_muon_step", "mc_muon_workspace_size", "mc_gemm_bf16",
+    "mc_launch_count", "mc_trace_enable", "mc_trace_collect",
+    "MC_F32", "MC_BF16", "MC_DEV_NONFINITE", "MC_DEV_TIMEOUT", "MC_DEV_RANGE", "NS_COEFFS",
+]
+
+MC_F32, MC_BF16 = 0, 1
+MC_DEV_NONFINITE, MC_DEV_TIMEOUT, MC_DEV_RANGE = 0x1, 0x2, 0x4
+# quintic Newton-Schulz coefficients ("Notes on Muon blog", "Algorithm")
+NS_COEFFS = (3.4445, -4.7750, 2.0315)
+
+_HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                       "include", "mc_max.h")
+
+
+class MCError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} failed: {msg} (status {status})")
+        self.status = status
+
+
+class TraceEntry(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_longlong),
+                ("total_ms", ctypes.c_double)]
+
+
+class MlaLayer(ctypes.Structure):
+    _fields_ = [("D", ctypes.c_int), ("q_lora", ctypes.c_int), ("kv_lora", ctypes.c_int),
+                ("H", ctypes.c_int), ("nope", ctypes.c_int), ("rope", ctypes.c_int),
+                ("rope_base", ctypes.c_float), ("wtype", ctypes.c_int),
+                ("w_qa", ctypes.c_void_p), ("w_qb", ctypes.c_void_p),
+                ("w_kva", ctypes.c_void_p), ("w_kb", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def header_symbols() -> list[str]:
+    """Names of every function declared in include/mc_max.h."""
+    with open(_HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(mc_\w+)\s*\(", text, re.M)))
+
+
+def load_library():
+    """Load libmc_max.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with muonclip_mc_max_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    V, I, F, S, U = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_uint
+    IP = ctypes.POINTER(ctypes.c_int)
+    VP = ctypes.POINTER(ctypes.c_void_p)
+    sig = {
+        "mc_status_string": ([I], ctypes.c_char_p),
+        "mc_read_device_status": ([V, ctypes.POINTER(U), I], I),
+        "mc_max_logits_mha_workspace_size": ([I, I, I, I, I, I], S),
+        "mc_max_logits_mha": ([V, V, V, I, I, I, I, I, I, I, I, V, V, V, S, V], I),
+        "mc_max_logits_mla_workspace_size": ([ctypes.POINTER(MlaLayer), I, I], S),
+        "mc_max_logits_mla": ([ctypes.POINTER(MlaLayer), V, I, I, I, I, V, V, V, S, V], I),
+        "mc_qk_clip_mha": ([V, V, I, I, I, I, V, F, V, V], I),
+        "mc_qk_clip_mla": ([ctypes.POINTER(MlaLayer), V, F, V, V], I),
+        "mc_qk_clip_global": ([V, V, I, I, I, V, I, F, F, V, V], I),
+        "mc_newton_schulz_workspace_size": ([IP, IP, I], S),
+        "mc_muon_workspace_size": ([IP, IP, I], S),
+        "mc_newton_schulz": ([VP, VP, IP, IP, I, I, F, F, F, F, V, S, V], I),
+        "mc_muon_step": ([VP, VP, VP, IP, IP, I, F, F, F, F, I, F, F, F, F, I, V, S, V], I),
+        "mc_gemm_bf16": ([V, V, V, I, I, I, I, I, I, V], I),
+        "mc_launch_count": ([], ctypes.c_ulonglong),
+        "mc_trace_enable": ([I], I),
+        "mc_trace_collect": ([ctypes.POINTER(TraceEntry), I], I),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def mc_status_string(status: int) -> str:
+    return load_library().mc_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise MCError(fn, status, mc_status_string(status))
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return MC_BF16
+    if t.dtype == torch.float32:
+        return MC_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("tensor must be on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("tensor must be contiguous")
+
+
+class Workspace:
+    """A growable device byte buffer handed to the library as scratch."""
+
+    def __init__(self, device=None):
+        self.device = device
+        self.buf = None
+
+    def get(self, nbytes: int, device) -> torch.Tensor:
+        nbytes = max(int(nbytes), 256)
+        if self.buf is None or self.buf.numel() < nbytes or self.buf.device != device:
+            self.buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        return self.buf
+
+
+_default_ws: dict = {}
+
+
+def _ws(workspace, nbytes, device):
+    if workspace is None:
+        workspace = _default_ws.setdefault(str(device), Workspace())
+    buf = workspace.get(nbytes, device)
+    return ctypes.c_void_p(buf.data_ptr()), buf.numel()
+
+
+def mc_read_device_status(clear: bool = True, stream=None) -> int:
+    bits = ctypes.c_uint(0)
+    _check("mc_read_device_status",
+           load_library().mc_read_device_status(_stream(stream), ctypes.byref(bits), int(clear)))
+    return bits.value
+
+
+# ---------------------------------------------------------------------------
+# (1) max logits
+# ---------------------------------------------------------------------------
+
+def mc_max_logits_mha_workspace_size(B, T, D, H, dh, dtype=MC_BF16) -> int:
+    return load_library().mc_max_logits_mha_workspace_size(B, T, D, H, dh, dtype)
+
+
+def mc_max_logits_mha(x, wq, wk, H: int, dh: int, causal: bool = False, accumulate: bool = False,
+                      s_max=None, s_max_bh=None, workspace=None, stream=None):
+    """x [B,T,D], wq/wk [D,H*dh] (bf16 or f32).  Returns s_max [H] f32."""
+    lib = load_library()
+    _need_cuda(x, wq, wk, s_max, s_max_bh)
+    B, T, D = x.shape
+    if wq.shape != (D, H * dh) or wk.shape != (D, H * dh):
+        raise ValueError("wq, wk must be [D, H*dh]")
+    dt = _dtype(x)
+    if s_max is None:
+        s_max = torch.empty(H, dtype=torch.float32, device=x.device)
+    ws, nb = _ws(workspace, lib.mc_max_logits_mha_workspace_size(B, T, D, H, dh, dt), x.device)
+    _check("mc_max_logits_mha", lib.mc_max_logits_mha(
+        _ptr(x), _ptr(wq), _ptr(wk), dt, B, T, D, H, dh, int(causal), int(accumulate),
+        _ptr(s_max), _ptr(s_max_bh), ws, nb, _stream(stream)))
+    return s_max
+
+
+def _mla_layer(w_qa, w_qb, w_kva, w_kb, H, nope, rope, rope_base, D=None, q_lora=None,
+               kv_lora=None, wtype=None):
+    L = MlaLayer()
+    L.D = D if D is not None else (w_qa.shape[0] if w_qa is not None else 0)
+    L.q_lora = q_lora if q_lora is not None else w_qb.shape[0]
+    L.kv_lora = kv_lora if kv_lora is not None else w_kb.shape[0]
+    L.H, L.nope, L.rope = H, nope, rope
+    L.rope_base = rope_base
+    L.wtype = wtype if wtype is not None else _dtype(w_qb)
+    L.w_qa = None if w_qa is None else w_qa.data_ptr()
+    L.w_qb = w_qb.data_ptr()
+    L.w_kva = None if w_kva is None else w_kva.data_ptr()
+    L.w_kb = w_kb.data_ptr()
+    return L
+
+
+def mc_max_logits_mla_workspace_size(layer: MlaLayer, B: int, T: int) -> int:
+    return load_library().mc_max_logits_mla_workspace_size(ctypes.byref(layer), B, T)
+
+
+def mc_max_logits_mla(x, w_qa, w_qb, w_kva, w_kb, H: int, nope: int, rope: int,
+                      rope_base: float = 50000.0, causal: bool = True, accumulate: bool = False,
+                      s_max=None, s_max_bh=None, workspace=None, stream=None):
+    """MLA per-head max logit; shapes as in mc_mla_layer.  Returns s_max [H]."""
+    lib = load_library()
+    _need_cuda(x, w_qa, w_qb, w_kva, w_kb, s_max, s_max_bh)
+    B, T, D = x.shape
+    L = _mla_layer(w_qa, w_qb, w_kva, w_kb, H, nope, rope, rope_base)
+    if s_max is None:
+        s_max = torch.empty(H, dtype=torch.float32, device=x.device)
+    ws, nb = _ws(workspace, lib.mc_max_logits_mla_workspace_size(ctypes.byref(L), B, T), x.device)
+    _check("mc_max_logits_mla", lib.mc_max_logits_mla(
+        ctypes.byref(L), _ptr(x), B, T, int(causal), int(accumulate), _ptr(s_max),
+        _ptr(s_max_bh), ws, nb, _stream(stream)))
+    return s_max
+
+
+# ---------------------------------------------------------------------------
+# (2) QK-Clip
+# ---------------------------------------------------------------------------
+
+def mc_qk_clip_mha(wq, wk, H: int, dh: int, s_max, tau: float, gamma=None, stream=None):
+    """In-place MHA clip; returns gamma [H]."""
+    lib = load_library()
+    _need_cuda(wq, wk, s_max, gamma)
+    if gamma is None:
+        gamma = torch.empty(H, dtype=torch.float32, device=wq.device)
+    D = wq.shape[0]
+    _check("mc_qk_clip_mha", lib.mc_qk_clip_mha(_ptr(wq), _ptr(wk), _dtype(wq), D, H, dh,
+                                                _ptr(s_max), float(tau), _ptr(gamma),
+                                                _stream(stream)))
+    return gamma
+
+
+def mc_qk_clip_mla(w_qb, w_kb, H: int, nope: int, rope: int, s_max, tau: float, gamma=None,
+                   stream=None):
+    """In-place MLA clip of W_qb (q^C, q^R) and W_kb (k^C); returns gamma."""
+    lib = load_library()
+    _need_cuda(w_qb, w_kb, s_max, gamma)
+    if gamma is None:
+        gamma = torch.empty(H, dtype=torch.float32, device=w_qb.device)
+    L = _mla_layer(None, w_qb, None, w_kb, H, nope, rope, 0.0, D=1)
+    _check("mc_qk_clip_mla", lib.mc_qk_clip_mla(ctypes.byref(L), _ptr(s_max), float(tau),
+                                                _ptr(gamma), _stream(stream)))
+    return gamma
+
+
+def mc_qk_clip_global(wq, wk, s_max, tau: float, alpha: float = 0.5, gamma=None, stream=None):
+    lib = load_library()
+    _need_cuda(wq, wk, s_max, gamma)
+    if gamma is None:
+        gamma = torch.empty(1, dtype=torch.float32, device=wq.device)
+    rows, cols = wq.shape
+    _check("mc_qk_clip_global", lib.mc_qk_clip_global(
+        _ptr(wq), _ptr(wk), _dtype(wq), rows, cols, _ptr(s_max), s_max.numel(), float(tau),
+        float(alpha), _ptr(gamma), _stream(stream)))
+    return gamma
+
+
+# ---------------------------------------------------------------------------
+# (3) Muon
+# ---------------------------------------------------------------------------
+
+def _shapes(mats):
+    n = len(mats)
+    rows = (ctypes.c_int * n)(*[m.shape[0] for m in mats])
+    cols = (ctypes.c_int * n)(*[m.shape[1] for m in mats])
+    return rows, cols
+
+
+def _ptrs(mats):
+    return (ctypes.c_void_p * len(mats))(*[m.data_ptr() for m in mats])
+
+
+def mc_newton_schulz_workspace_size(shapes) -> int:
+    n = len(shapes)
+    rows = (ctypes.c_int * n)(*[s[0] for s in shapes])
+    cols = (ctypes.c_int * n)(*[s[1] for s in shapes])
+    return load_library().mc_newton_schulz_workspace_size(rows, cols, n)
+
+
+def mc_muon_workspace_size(shapes) -> int:
+    n = len(shapes)
+    rows = (ctypes.c_int * n)(*[s[0] for s in shapes])
+    cols = (ctypes.c_int * n)(*[s[1] for s in shapes])
+    return load_library().mc_muon_workspace_size(rows, cols, n)
+
+
+def mc_newton_schulz(mats, steps: int = 5, coeffs=NS_COEFFS, eps: float = 1e-7, out=None,
+                     workspace=None, stream=None):
+    """Newton-Schulz of each f32 matrix; returns a list of f32 outputs."""
+    lib = load_library()
+    _need_cuda(*mats)
+    if out is None:
+        out = [torch.empty_like(m) for m in mats]
+    _need_cuda(*out)
+    rows, cols = _shapes(mats)
+    n = len(mats)
+    ws, nb = _ws(workspace, lib.mc_newton_schulz_workspace_size(rows, cols, n), mats[0].device)
+    a, b, c = coeffs
+    _check("mc_newton_schulz", lib.mc_newton_schulz(
+        _ptrs(mats), _ptrs(out), rows, cols, n, steps, a, b, c, eps, ws, nb, _stream(stream)))
+    return out
+
+
+def mc_muon_step(w, g, m, lr: float, mu: float = 0.95, wd: float = 0.1, rms: float = 0.2,
+                 steps: int = 5, coeffs=NS_COEFFS, eps: float = 1e-7, nesterov: bool = False,
+                 workspace=None, stream=None):
+    """One in-place Muon step over lists of f32 weights, grads, momenta."""
+    lib = load_library()
+    _need_cuda(*w, *g, *m)
+    rows, cols = _shapes(w)
+    n = len(w)
+    ws, nb = _ws(workspace, lib.mc_muon_workspace_size(rows, cols, n), w[0].device)
+    a, b, c = coeffs
+    _check("mc_muon_step", lib.mc_muon_step(
+        _ptrs(w), _ptrs(g), _ptrs(m), rows, cols, n, lr, mu, wd, rms, steps, a, b, c, eps,
+        int(nesterov), ws, nb, _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# tensor-core GEMM
+# ---------------------------------------------------------------------------
+
+def mc_gemm_bf16(a, b, b_kmajor: bool = True, out_dtype=torch.float32, out=None, stream=None):
+    """a [(Z,)M,K] bf16; b [(Z,)N,K] (b_kmajor) or [(Z,)K,N]; returns [(Z,)M,N]."""
+    lib = load_library()
+    _need_cuda(a, b)
+    batched = a.dim() == 3
+    A = a if batched else a.unsqueeze(0)
+    Bt = b if batched else b.unsqueeze(0)
+    Z, M, K = A.shape
+    N = Bt.shape[1] if b_kmajor else Bt.shape[2]
+    if out is None:
+        out = torch.empty((Z, M, N), dtype=out_dtype, device=a.device)
+    _need_cuda(out)
+    ct = MC_F32 if out.dtype == torch.float32 else MC_BF16
+    _check("mc_gemm_bf16", lib.mc_gemm_bf16(_ptr(A), _ptr(Bt), _ptr(out), ct, M, N, K, Z,
+                                            int(b_kmajor), _stream(stream)))
+    return out if batched else out[0]
+
+
+# ---------------------------------------------------------------------------
+# tracing
+# ---------------------------------------------------------------------------
+
+def mc_launch_count() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(load_library().mc_launch_count())
+
+
+def mc_trace_enable(on: bool = True):
+    _check("mc_trace_enable", load_library().mc_trace_enable(int(on)))
+
+
+def mc_trace_collect() -> dict:
+    """{kernel kind: (launches, total_ms)} of the launches traced since the
+    last collect (event-timed on their launch streams)."""
+    lib = load_library()
+    cap = 64
+    buf = (TraceEntry * cap)()
+    n = lib.mc_trace_collect(buf, cap)
+    if n < 0:
+        raise MCError("mc_trace_collect", 3, "CUDA error while reading trace events")
+    return {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms))
+            for i in range(min(n, cap))}

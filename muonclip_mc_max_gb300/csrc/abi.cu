@@ -1,0 +1,835 @@
+// abi.cu -- the C ABI of include/mc_max.h: argument checks, workspace
+// carving, tensor-map encoding and launch sequencing on the caller's stream.
+// No device memory is allocated here; every buffer is the caller's.
+#include <algorithm>
+#include <atomic>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace mc {
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+__device__ unsigned g_status_word;  // per-device status bits (MC_DEV_*)
+
+static std::mutex g_mu;
+static unsigned* g_status_ptr[64];
+static int g_sms[64];
+
+int current_device() {
+    int d = -1;
+    if (cudaGetDevice(&d) != cudaSuccess) return -1;
+    return d;
+}
+
+unsigned* device_status_ptr() {
+    int dev = current_device();
+    if (dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) == cudaSuccess) g_status_ptr[dev] = (unsigned*)p;
+    }
+    return g_status_ptr[dev];
+}
+
+int num_sms() {
+    int dev = current_device();
+    if (dev < 0 || dev >= 64) return 1;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_sms[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        g_sms[dev] = n > 0 ? n : 1;
+    }
+    return g_sms[dev];
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+bool make_tmap_3d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, uint64_t batch,
+                  uint64_t outer_stride, uint64_t batch_stride, uint32_t box_inner, uint32_t box_outer, int f16) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || !base || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
+    if (batch == 1) batch_stride = outer_stride * outer;
+    cuuint64_t dims[3] = {inner, outer, batch};
+    cuuint64_t strides[2] = {outer_stride * 2, batch_stride * 2};
+    if ((strides[0] & 15) || (strides[1] & 15)) return false;
+    cuuint32_t box[3] = {box_inner, box_outer, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(tm, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+void finalize_gemm_params(GemmParams& P) {
+    int begin = 0;
+    for (int i = 0; i < P.nprob; ++i) {
+        GemmProblem& q = P.p[i];
+        q.tiles_m = (q.M + kBM - 1) / kBM;
+        q.tiles_n = (q.N + kBN - 1) / kBN;
+        if (q.sym) {
+            int t = 0;
+            for (int tm = 0; tm < q.tiles_m; ++tm) t += q.tiles_n - tm / 2;
+            q.tiles_per_batch = t;
+        } else {
+            q.tiles_per_batch = q.tiles_m * q.tiles_n;
+        }
+        q.tile_begin = begin;
+        begin += q.tiles_per_batch * q.batch;
+    }
+    P.total_tiles = begin;
+    P.status = device_status_ptr();
+}
+
+// ---------------------------------------------------------------------------
+// launch counting and optional event tracing
+// ---------------------------------------------------------------------------
+static std::atomic<unsigned long long> g_launches{0};
+static std::atomic<int> g_trace_on{0};
+struct TraceRec {
+    const char* name;
+    cudaEvent_t a, b;
+};
+static std::mutex g_trace_mu;
+static std::vector<TraceRec> g_trace;
+static std::vector<cudaEvent_t> g_event_pool;
+
+static cudaEvent_t pooled_event() {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+TraceScope::TraceScope(const char* name, cudaStream_t stream) : name_(name), stream_(stream), start_(nullptr) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (g_trace_on.load(std::memory_order_relaxed)) {
+        start_ = pooled_event();
+        if (start_) cudaEventRecord(start_, stream_);
+    }
+}
+
+TraceScope::~TraceScope() {
+    if (!start_) return;
+    cudaEvent_t end = pooled_event();
+    if (!end) return;
+    cudaEventRecord(end, stream_);
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    g_trace.push_back(TraceRec{name_, start_, end});
+}
+
+static size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+
+// bump allocator over the caller's workspace
+struct Carve {
+    uint8_t* base;
+    size_t used;
+    template <typename T>
+    T* take(size_t count) {
+        T* p = base ? reinterpret_cast<T*>(base + used) : nullptr;
+        used += align256(count * sizeof(T));
+        return p;
+    }
+};
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Projection D = A W with W [K][N] row-major (the MN-major B operand);
+// A and W both bf16 (f16 = 0) or both fp16 (f16 = 1); D stored in fp16.
+static bool weight_problem(GemmProblem& q, const void* a, int64_t a_rows, int64_t a_inner, int64_t a_ld,
+                           const void* w, int64_t K, int64_t N, void* out, int64_t out_ld, int f16) {
+    memset(&q, 0, sizeof(q));
+    if (!make_tmap_3d(&q.tmA, a, a_inner, a_rows, 1, a_ld, 0, kBK, kBM, f16)) return false;
+    if (!make_tmap_3d(&q.tmB, w, N, K, 1, N, 0, 64, kBK, f16)) return false;
+    q.ab_f16 = f16;
+    q.out_kind = kOutF16;
+    q.M = (int)a_rows;
+    q.N = (int)N;
+    q.K = (int)K;
+    q.batch = 1;
+    q.b_mn = 1;
+    q.out = out;
+    q.out_ld = out_ld;
+    q.out_bstride = 0;
+    q.alpha = 1.f;
+    q.beta = 0.f;
+    q.vec_ok = (out_ld % 8 == 0) && aligned16(out);
+    return true;
+}
+
+}  // namespace mc
+
+using namespace mc;
+
+#define MC_CUDA(call)                                  \
+    do {                                               \
+        cudaError_t e_ = (call);                       \
+        if (e_ != cudaSuccess) return MC_ERR_CUDA;     \
+    } while (0)
+
+extern "C" {
+
+const char* mc_status_string(mc_status s) {
+    switch (s) {
+        case MC_OK: return "ok";
+        case MC_ERR_INVALID_ARG: return "invalid argument";
+        case MC_ERR_UNSUPPORTED: return "unsupported shape or type";
+        case MC_ERR_CUDA: return "CUDA error";
+        case MC_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    }
+    return "unknown status";
+}
+
+mc_status mc_read_device_status(mc_stream_t stream, unsigned* bits, int clear) {
+    if (!bits) return MC_ERR_INVALID_ARG;
+    MC_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+    unsigned* p = device_status_ptr();
+    if (!p) return MC_ERR_CUDA;
+    MC_CUDA(cudaMemcpy(bits, p, sizeof(unsigned), cudaMemcpyDeviceToHost));
+    if (clear) MC_CUDA(cudaMemset(p, 0, sizeof(unsigned)));
+    return MC_OK;
+}
+
+unsigned long long mc_launch_count(void) { return g_launches.load(); }
+
+mc_status mc_trace_enable(int on) {
+    g_trace_on.store(on ? 1 : 0);
+    return MC_OK;
+}
+
+int mc_trace_collect(mc_trace_entry* out, int cap) {
+    std::vector<TraceRec> recs;
+    {
+        std::lock_guard<std::mutex> lk(g_trace_mu);
+        recs.swap(g_trace);
+    }
+    std::map<std::string, std::pair<long long, double>> agg;
+    std::vector<std::string> order;
+    int rc = 0;
+    for (auto& r : recs) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) rc = -1;
+        auto it = agg.find(r.name);
+        if (it == agg.end()) {
+            order.push_back(r.name);
+            agg[r.name] = {1, (double)ms};
+        } else {
+            it->second.first += 1;
+            it->second.second += ms;
+        }
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_trace_mu);
+        for (auto& r : recs) {
+            g_event_pool.push_back(r.a);
+            g_event_pool.push_back(r.b);
+        }
+    }
+    if (rc) return -1;
+    int n = 0;
+    for (auto& name : order) {
+        if (out && n < cap) {
+            memset(out[n].name, 0, sizeof(out[n].name));
+            strncpy(out[n].name, name.c_str(), sizeof(out[n].name) - 1);
+            out[n].launches = agg[name].first;
+            out[n].total_ms = agg[name].second;
+        }
+        ++n;
+    }
+    return n;
+}
+
+// ===========================================================================
+// (1) max-logit scan
+// ===========================================================================
+
+static bool mha_tensor_path(mc_dtype dt, int D, int dh) { return dt == MC_BF16 && D % 8 == 0 && dh % 64 == 0 && dh <= 192; }
+
+static size_t mha_carve(Carve& c, int B, int T, int D, int H, int dh, mc_dtype dt, void** q, void** k,
+                        unsigned** keys) {
+    size_t n = (size_t)B * T * H * dh;
+    if (mha_tensor_path(dt, D, dh)) {
+        *q = c.take<__half>(n);
+        *k = c.take<__half>(n);
+    } else {
+        *q = c.take<float>(n);
+        *k = c.take<float>(n);
+    }
+    *keys = c.take<unsigned>((size_t)B * H);
+    return c.used;
+}
+
+size_t mc_max_logits_mha_workspace_size(int B, int T, int D, int H, int dh, mc_dtype dtype) {
+    if (B <= 0 || T <= 0 || D <= 0 || H <= 0 || dh <= 0) return 0;
+    Carve c{nullptr, 0};
+    void *q, *k;
+    unsigned* keys;
+    return mha_carve(c, B, T, D, H, dh, dtype, &q, &k, &keys);
+}
+
+mc_status mc_max_logits_mha(const void* x, const void* wq, const void* wk, mc_dtype dtype, int B, int T, int D,
+                            int H, int dh, int causal, int accumulate, float* s_max, float* s_max_bh, void* ws,
+                            size_t ws_bytes, mc_stream_t stream_) {
+    cudaStream_t stream = (cudaStream_t)stream_;
+    if (!x || !wq || !wk || !s_max) return MC_ERR_INVALID_ARG;
+    if (B <= 0 || T <= 0 || D <= 0 || H <= 0 || dh <= 0) return MC_ERR_INVALID_ARG;
+    if (dtype != MC_F32 && dtype != MC_BF16) return MC_ERR_INVALID_ARG;
+    if ((int64_t)B * T > INT32_MAX || (int64_t)H * dh > INT32_MAX) return MC_ERR_UNSUPPORTED;
+    size_t need = mc_max_logits_mha_workspace_size(B, T, D, H, dh, dtype);
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < need) return MC_ERR_WORKSPACE;
+    Carve c{(uint8_t*)ws, 0};
+    void *q, *k;
+    unsigned* keys;
+    mha_carve(c, B, T, D, H, dh, dtype, &q, &k, &keys);
+    MC_CUDA(cudaMemsetAsync(keys, 0, sizeof(unsigned) * B * H, stream));
+    const int64_t BT = (int64_t)B * T, N = (int64_t)H * dh;
+    if (mha_tensor_path(dtype, D, dh)) {
+        if (!aligned16(x) || !aligned16(wq) || !aligned16(wk)) return MC_ERR_INVALID_ARG;
+        GemmParams P;
+        memset(&P, 0, sizeof(P));
+        P.nprob = 2;
+        if (!weight_problem(P.p[0], x, BT, D, D, wq, D, N, q, N, 0)) return MC_ERR_INVALID_ARG;
+        if (!weight_problem(P.p[1], x, BT, D, D, wk, D, N, k, N, 0)) return MC_ERR_INVALID_ARG;
+        finalize_gemm_params(P);
+        MC_CUDA(launch_gemm(P, stream, "gemm:proj"));
+        ScanArgs a;
+        memset(&a, 0, sizeof(a));
+        a.q = q;
+        a.q_ld = N;
+        a.k = k;
+        a.k_ld = N;
+        a.B = B;
+        a.T = T;
+        a.H = H;
+        a.causal = causal ? 1 : 0;
+        a.q_head_stride = dh;
+        a.k_head_stride = dh;
+        a.nkb_main = dh / 64;
+        a.nkb_rope = 0;
+        a.keys = keys;
+        MC_CUDA(launch_scan(a, stream));
+    } else {
+        MC_CUDA(launch_proj_simt(x, wq, dtype, (float*)q, (int)BT, D, (int)N, stream));
+        MC_CUDA(launch_proj_simt(x, wk, dtype, (float*)k, (int)BT, D, (int)N, stream));
+        MC_CUDA(launch_scan_simt((const float*)q, (const float*)k, B, T, H, dh, causal ? 1 : 0, keys, stream));
+    }
+    MC_CUDA(launch_finalize_smax(keys, B, H, (float)dh, accumulate, s_max, s_max_bh, stream));
+    return MC_OK;
+}
+
+static mc_status mla_check(const mc_mla_layer* L, bool scan) {
+    if (!L) return MC_ERR_INVALID_ARG;
+    if (L->D <= 0 || L->q_lora <= 0 || L->kv_lora <= 0 || L->H <= 0 || L->nope < 0 || L->rope < 0)
+        return MC_ERR_INVALID_ARG;
+    if (!L->w_qb || !L->w_kb) return MC_ERR_INVALID_ARG;
+    if (L->wtype != MC_BF16 && L->wtype != MC_F32) return MC_ERR_INVALID_ARG;
+    if (scan) {
+        if (!L->w_qa || !L->w_kva) return MC_ERR_INVALID_ARG;
+        if (L->wtype != MC_BF16 || L->rope != 64 || L->nope % 64 || L->nope <= 0 || L->nope + L->rope > 192 ||
+            L->D % 64 || L->q_lora % 64 || L->kv_lora % 64)
+            return MC_ERR_UNSUPPORTED;
+    }
+    return MC_OK;
+}
+
+struct MlaWs {
+    float2* rope;
+    __half *cq, *ckv, *q, *kc, *wqb, *wkb;  // fp16 intermediates and fp16 copies of W_qb, W_kb
+    unsigned* keys;
+};
+
+static size_t mla_carve(Carve& c, const mc_mla_layer* L, int B, int T, MlaWs& w) {
+    size_t BT = (size_t)B * T;
+    w.rope = c.take<float2>((size_t)T * 32);
+    w.cq = c.take<__half>(BT * L->q_lora);
+    w.ckv = c.take<__half>(BT * (L->kv_lora + L->rope));
+    w.q = c.take<__half>(BT * (size_t)L->H * (L->nope + L->rope));
+    w.kc = c.take<__half>(BT * (size_t)L->H * L->nope);
+    w.wqb = c.take<__half>((size_t)L->q_lora * L->H * (L->nope + L->rope));
+    w.wkb = c.take<__half>((size_t)L->kv_lora * L->H * L->nope);
+    w.keys = c.take<unsigned>((size_t)B * L->H);
+    return c.used;
+}
+
+size_t mc_max_logits_mla_workspace_size(const mc_mla_layer* L, int B, int T) {
+    if (!L || B <= 0 || T <= 0 || L->H <= 0) return 0;
+    Carve c{nullptr, 0};
+    MlaWs w;
+    return mla_carve(c, L, B, T, w);
+}
+
+mc_status mc_max_logits_mla(const mc_mla_layer* L, const void* x, int B, int T, int causal, int accumulate,
+                            float* s_max, float* s_max_bh, void* ws, size_t ws_bytes, mc_stream_t stream_) {
+    cudaStream_t stream = (cudaStream_t)stream_;
+    mc_status st = mla_check(L, true);
+    if (st != MC_OK) return st;
+    if (!x || !s_max || B <= 0 || T <= 0) return MC_ERR_INVALID_ARG;
+    if ((int64_t)B * T > INT32_MAX) return MC_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(L->w_qa) || !aligned16(L->w_qb) || !aligned16(L->w_kva) || !aligned16(L->w_kb))
+        return MC_ERR_INVALID_ARG;
+    size_t need = mc_max_logits_mla_workspace_size(L, B, T);
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < need) return MC_ERR_WORKSPACE;
+    Carve c{(uint8_t*)ws, 0};
+    MlaWs w;
+    mla_carve(c, L, B, T, w);
+    const int64_t BT = (int64_t)B * T;
+    const int qk = L->nope + L->rope, kvw = L->kv_lora + L->rope;
+    MC_CUDA(cudaMemsetAsync(w.keys, 0, sizeof(unsigned) * B * L->H, stream));
+    MC_CUDA(launch_rope_table(w.rope, T, L->rope_base, stream));
+    // phase 1: c_Q = x W_qa ; [c_KV | k^R] = x W_kva (RoPE on the k^R columns)
+    GemmParams P;
+    memset(&P, 0, sizeof(P));
+    P.nprob = 2;
+    if (!weight_problem(P.p[0], x, BT, L->D, L->D, L->w_qa, L->D, L->q_lora, w.cq, L->q_lora, 0))
+        return MC_ERR_INVALID_ARG;
+    if (!weight_problem(P.p[1], x, BT, L->D, L->D, L->w_kva, L->D, kvw, w.ckv, kvw, 0)) return MC_ERR_INVALID_ARG;
+    P.p[1].rope_tab = w.rope;
+    P.p[1].rope_T = T;
+    P.p[1].rope_period = kvw;
+    P.p[1].rope_start = L->kv_lora;
+    finalize_gemm_params(P);
+    MC_CUDA(launch_gemm(P, stream, "gemm:proj"));
+    // phase 2: [q^C | q^R] = c_Q W_qb (RoPE on q^R) ; k^C = c_KV W_kb, on
+    // fp16 operands (W_qb, W_kb converted; exact in fp16's normal range)
+    const int64_t Nq = (int64_t)L->H * qk, Nk = (int64_t)L->H * L->nope;
+    MC_CUDA(launch_bf16_to_f16(L->w_qb, w.wqb, (long long)L->q_lora * Nq, stream));
+    MC_CUDA(launch_bf16_to_f16(L->w_kb, w.wkb, (long long)L->kv_lora * Nk, stream));
+    memset(&P, 0, sizeof(P));
+    P.nprob = 2;
+    if (!weight_problem(P.p[0], w.cq, BT, L->q_lora, L->q_lora, w.wqb, L->q_lora, Nq, w.q, Nq, 1))
+        return MC_ERR_INVALID_ARG;
+    P.p[0].rope_tab = w.rope;
+    P.p[0].rope_T = T;
+    P.p[0].rope_period = qk;
+    P.p[0].rope_start = L->nope;
+    if (!weight_problem(P.p[1], w.ckv, BT, L->kv_lora, kvw, w.wkb, L->kv_lora, Nk, w.kc, Nk, 1))
+        return MC_ERR_INVALID_ARG;
+    finalize_gemm_params(P);
+    MC_CUDA(launch_gemm(P, stream, "gemm:proj"));
+    // scan: per head 3 K blocks (q^C.k^C x2, q^R.k^R x1)
+    ScanArgs a;
+    memset(&a, 0, sizeof(a));
+    a.q = w.q;
+    a.q_ld = Nq;
+    a.k = w.kc;
+    a.k_ld = Nk;
+    a.kr = w.ckv;
+    a.kr_ld = kvw;
+    a.B = B;
+    a.T = T;
+    a.H = L->H;
+    a.causal = causal ? 1 : 0;
+    a.q_head_stride = qk;
+    a.k_head_stride = L->nope;
+    a.nkb_main = L->nope / 64;
+    a.nkb_rope = 1;
+    a.kr_col = L->kv_lora;
+    a.keys = w.keys;
+    MC_CUDA(launch_scan(a, stream));
+    MC_CUDA(launch_finalize_smax(w.keys, B, L->H, (float)qk, accumulate, s_max, s_max_bh, stream));
+    return MC_OK;
+}
+
+// ===========================================================================
+// (2) QK-Clip
+// ===========================================================================
+
+mc_status mc_qk_clip_mha(void* wq, void* wk, mc_dtype dtype, int D, int H, int dh, const float* s_max, float tau,
+                         float* gamma, mc_stream_t stream) {
+    if (!wq || !wk || !s_max || D <= 0 || H <= 0 || dh <= 0) return MC_ERR_INVALID_ARG;
+    if (dtype != MC_F32 && dtype != MC_BF16) return MC_ERR_INVALID_ARG;
+    ClipArgs a;
+    memset(&a, 0, sizeof(a));
+    a.nseg = 2;
+    a.H = H;
+    a.bf16 = dtype == MC_BF16;
+    a.s_max = s_max;
+    a.tau = tau;
+    a.gamma_out = gamma;
+    for (int s = 0; s < 2; ++s) {
+        a.seg[s].w = s ? wk : wq;
+        a.seg[s].ld = (long long)H * dh;
+        a.seg[s].rows = D;
+        a.seg[s].col0 = 0;
+        a.seg[s].head_stride = dh;
+        a.seg[s].width = dh;
+        a.seg[s].use_gamma = 0;
+    }
+    MC_CUDA(launch_clip(a, (cudaStream_t)stream));
+    return MC_OK;
+}
+
+mc_status mc_qk_clip_mla(const mc_mla_layer* L, const float* s_max, float tau, float* gamma, mc_stream_t stream) {
+    mc_status st = mla_check(L, false);
+    if (st != MC_OK) return st;
+    if (!s_max) return MC_ERR_INVALID_ARG;
+    const int qk = L->nope + L->rope;
+    ClipArgs a;
+    memset(&a, 0, sizeof(a));
+    a.H = L->H;
+    a.bf16 = L->wtype == MC_BF16;
+    a.s_max = s_max;
+    a.tau = tau;
+    a.gamma_out = gamma;
+    int n = 0;
+    if (L->nope > 0) {  // q^C x sqrt(gamma)
+        a.seg[n++] = ClipSeg{L->w_qb, (long long)L->H * qk, L->q_lora, 0, qk, L->nope, 0};
+    }
+    if (L->rope > 0) {  // q^R x gamma
+        a.seg[n++] = ClipSeg{L->w_qb, (long long)L->H * qk, L->q_lora, L->nope, qk, L->rope, 1};
+    }
+    if (L->nope > 0) {  // k^C x sqrt(gamma)
+        a.seg[n++] = ClipSeg{L->w_kb, (long long)L->H * L->nope, L->kv_lora, 0, L->nope, L->nope, 0};
+    }
+    a.nseg = n;
+    if (n == 0) return MC_OK;
+    MC_CUDA(launch_clip(a, (cudaStream_t)stream));
+    return MC_OK;
+}
+
+mc_status mc_qk_clip_global(void* wq, void* wk, mc_dtype dtype, int rows, int cols, const float* s_max, int H,
+                            float tau, float alpha, float* gamma_out, mc_stream_t stream) {
+    if (!wq || !wk || !s_max || rows <= 0 || cols <= 0 || H <= 0) return MC_ERR_INVALID_ARG;
+    if (dtype != MC_F32 && dtype != MC_BF16) return MC_ERR_INVALID_ARG;
+    MC_CUDA(launch_clip_global(wq, wk, dtype == MC_BF16, (long long)rows * cols, s_max, H, tau, alpha, gamma_out,
+                               (cudaStream_t)stream));
+    return MC_OK;
+}
+
+// ===========================================================================
+// (3) Muon
+// ===========================================================================
+
+namespace {
+
+struct NsGroup {
+    int m, n, m_pad, n_pad;
+    std::vector<int> idx;  // input indices
+    int zbase;             // position of idx[0] in the group-ordered list
+    __nv_bfloat16* X[2];
+    __nv_bfloat16* A;
+    __nv_bfloat16* Bm;
+};
+
+struct NsPlan {
+    std::vector<NsGroup> groups;
+    std::vector<int> order;      // group-ordered input indices
+    std::vector<double*> part;   // per ordered position
+    std::vector<int> nparts;
+    float* s;
+    float* s2;
+    size_t bytes;
+};
+
+int round_up(int v, int m) { return (v + m - 1) / m * m; }
+
+bool plan_ns(const int* rows, const int* cols, int count, uint8_t* base, NsPlan& P) {
+    P.groups.clear();
+    P.order.clear();
+    for (int i = 0; i < count; ++i) {
+        int m = std::min(rows[i], cols[i]), n = std::max(rows[i], cols[i]);
+        int mp = round_up(m, 256), np = round_up(n, 64);
+        int g = -1;
+        for (size_t j = 0; j < P.groups.size(); ++j)
+            if (P.groups[j].m_pad == mp && P.groups[j].n_pad == np) g = (int)j;
+        if (g < 0) {
+            NsGroup ng;
+            ng.m = m;
+            ng.n = n;
+            ng.m_pad = mp;
+            ng.n_pad = np;
+            P.groups.push_back(ng);
+            g = (int)P.groups.size() - 1;
+        }
+        P.groups[g].idx.push_back(i);
+    }
+    Carve c{base, 0};
+    for (auto& g : P.groups) {
+        g.zbase = (int)P.order.size();
+        for (int i : g.idx) P.order.push_back(i);
+        size_t cnt = g.idx.size();
+        g.X[0] = c.take<__nv_bfloat16>(cnt * g.m_pad * g.n_pad);
+        g.X[1] = c.take<__nv_bfloat16>(cnt * g.m_pad * g.n_pad);
+        g.A = c.take<__nv_bfloat16>(cnt * g.m_pad * g.m_pad);
+        g.Bm = c.take<__nv_bfloat16>(cnt * g.m_pad * g.m_pad);
+    }
+    P.part.assign(count, nullptr);
+    P.nparts.assign(count, 0);
+    for (auto& g : P.groups)
+        for (size_t k = 0; k < g.idx.size(); ++k) {
+            int np = (g.m_pad / 64) * (g.n_pad / 64);
+            P.part[g.zbase + k] = c.take<double>(np);
+            P.nparts[g.zbase + k] = np;
+        }
+    P.s = c.take<float>(count);
+    P.s2 = c.take<float>(count);
+    P.bytes = c.used;
+    return true;
+}
+
+bool valid_mats(const int* rows, const int* cols, int count) {
+    if (!rows || !cols || count <= 0) return false;
+    for (int i = 0; i < count; ++i) {
+        if (rows[i] <= 0 || cols[i] <= 0 || cols[i] % 4) return false;
+        if ((int64_t)rows[i] * cols[i] > ((int64_t)1 << 31)) return false;
+    }
+    return true;
+}
+
+// mode 0/1: momentum (+ cast) or cast; mode 2/3: update or write O
+mc_status run_mat_pass(const NsPlan& P, int mode, float* const* w, const float* const* g, float* const* m,
+                       const float* const* in, const int* rows, const int* cols, int xbuf, float mu, float lr,
+                       float wd, float rms_coef, int nesterov, bool zero_steps, cudaStream_t stream) {
+    const int count = (int)P.order.size();
+    // position -> group
+    std::vector<const NsGroup*> grp(count);
+    std::vector<int> within(count);
+    for (auto& gr : P.groups)
+        for (size_t k = 0; k < gr.idx.size(); ++k) {
+            grp[gr.zbase + k] = &gr;
+            within[gr.zbase + k] = (int)k;
+        }
+    for (int c0 = 0; c0 < count; c0 += kMaxBatchMats) {
+        MatBatch B;
+        memset(&B, 0, sizeof(B));
+        B.mode = mode;
+        B.mu = mu;
+        B.lr = lr;
+        B.wd = wd;
+        B.nesterov = nesterov;
+        int tiles = 0;
+        for (int p = c0; p < std::min(count, c0 + kMaxBatchMats); ++p) {
+            const int i = P.order[p];
+            const NsGroup& gr = *grp[p];
+            MatDesc& d = B.d[B.count++];
+            d.rows = rows[i];
+            d.cols = cols[i];
+            d.tr = rows[i] > cols[i];
+            d.m_pad = gr.m_pad;
+            d.n_pad = gr.n_pad;
+            d.x = gr.X[xbuf] + (size_t)within[p] * gr.m_pad * gr.n_pad;
+            d.partial = P.part[p];
+            d.tiles_x = gr.n_pad / 64;
+            d.tile_begin = tiles;
+            tiles += (gr.m_pad / 64) * (gr.n_pad / 64);
+            if (mode == 0) {
+                d.m = m[i];
+                d.g = g[i];
+            } else if (mode == 1) {
+                d.m = const_cast<float*>(in[i]);
+            } else {
+                d.w = w[i];
+                d.rms = rms_coef * sqrtf((float)std::max(rows[i], cols[i]));
+                d.oscale = zero_steps ? P.s + p : nullptr;
+            }
+        }
+        B.total_tiles = tiles;
+        MC_CUDA(launch_mat_pass(B, stream));
+    }
+    return MC_OK;
+}
+
+mc_status run_norm(const NsPlan& P, float eps, cudaStream_t stream) {
+    const int count = (int)P.order.size();
+    for (int c0 = 0; c0 < count; c0 += kMaxBatchMats) {
+        NormArgs a;
+        memset(&a, 0, sizeof(a));
+        a.eps = eps;
+        a.s = P.s + c0;
+        a.s2 = P.s2 + c0;
+        for (int p = c0; p < std::min(count, c0 + kMaxBatchMats); ++p) {
+            a.partial[a.count] = P.part[p];
+            a.nparts[a.count] = P.nparts[p];
+            ++a.count;
+        }
+        MC_CUDA(launch_norm_finalize(a, stream));
+    }
+    return MC_OK;
+}
+
+// kind 0: Gram A = sc2 X X^T ; 1: poly B = c A A + b A ; 2: apply X' = sc (B X + a X)
+mc_status run_ns_phase(const NsPlan& P, int kind, int it, float a, float b, float c, cudaStream_t stream) {
+    const int xin = it & 1, xout = (it + 1) & 1;
+    for (size_t g0 = 0; g0 < P.groups.size(); g0 += kMaxProblems) {
+        GemmParams G;
+        memset(&G, 0, sizeof(G));
+        for (size_t gi = g0; gi < std::min(P.groups.size(), g0 + kMaxProblems); ++gi) {
+            const NsGroup& gr = P.groups[gi];
+            GemmProblem& q = G.p[G.nprob++];
+            const uint64_t cnt = gr.idx.size(), mp = gr.m_pad, np = gr.n_pad;
+            q.batch = (int)cnt;
+            q.vec_ok = 1;
+            if (kind == 0) {
+                if (!make_tmap_3d(&q.tmA, gr.X[xin], np, mp, cnt, np, mp * np, kBK, kBM, 0)) return MC_ERR_CUDA;
+                if (!make_tmap_3d(&q.tmB, gr.X[xin], np, mp, cnt, np, mp * np, kBK, kBN, 0)) return MC_ERR_CUDA;
+                q.M = q.N = (int)mp;
+                q.K = (int)np;
+                q.sym = 1;
+                q.out = gr.A;
+                q.out_ld = mp;
+                q.out_bstride = mp * mp;
+                q.alpha = 1.f;
+                q.scale = it == 0 ? P.s2 + gr.zbase : nullptr;
+            } else if (kind == 1) {
+                if (!make_tmap_3d(&q.tmA, gr.A, mp, mp, cnt, mp, mp * mp, kBK, kBM, 0)) return MC_ERR_CUDA;
+                if (!make_tmap_3d(&q.tmB, gr.A, mp, mp, cnt, mp, mp * mp, kBK, kBN, 0)) return MC_ERR_CUDA;
+                q.M = q.N = q.K = (int)mp;
+                q.sym = 1;
+                q.out = gr.Bm;
+                q.out_ld = mp;
+                q.out_bstride = mp * mp;
+                q.aux = gr.A;
+                q.aux_ld = mp;
+                q.aux_bstride = mp * mp;
+                q.alpha = c;
+                q.beta = b;
+            } else {
+                if (!make_tmap_3d(&q.tmA, gr.Bm, mp, mp, cnt, mp, mp * mp, kBK, kBM, 0)) return MC_ERR_CUDA;
+                if (!make_tmap_3d(&q.tmB, gr.X[xin], np, mp, cnt, np, mp * np, 64, kBK, 0)) return MC_ERR_CUDA;
+                q.b_mn = 1;
+                q.M = (int)mp;
+                q.N = (int)np;
+                q.K = (int)mp;
+                q.out = gr.X[xout];
+                q.out_ld = np;
+                q.out_bstride = mp * np;
+                q.aux = gr.X[xin];
+                q.aux_ld = np;
+                q.aux_bstride = mp * np;
+                q.alpha = 1.f;
+                q.beta = a;
+                q.scale = it == 0 ? P.s + gr.zbase : nullptr;
+            }
+        }
+        static const char* kinds[3] = {"gemm:ns_gram", "gemm:ns_poly", "gemm:ns_apply"};
+        finalize_gemm_params(G);
+        MC_CUDA(launch_gemm(G, stream, kinds[kind]));
+    }
+    return MC_OK;
+}
+
+mc_status muon_impl(bool step, float* const* w, const float* const* g, float* const* m, const float* const* in,
+                    float* const* out, const int* rows, const int* cols, int count, float lr, float mu, float wd,
+                    float rms_coef, int steps, float a, float b, float c, float eps, int nesterov, void* ws,
+                    size_t ws_bytes, cudaStream_t stream) {
+    if (!valid_mats(rows, cols, count) || steps < 0) return MC_ERR_INVALID_ARG;
+    for (int i = 0; i < count; ++i) {
+        if (step) {
+            if (!w || !g || !m || !w[i] || !g[i] || !m[i]) return MC_ERR_INVALID_ARG;
+            if (!aligned16(w[i]) || !aligned16(g[i]) || !aligned16(m[i])) return MC_ERR_INVALID_ARG;
+        } else {
+            if (!in || !out || !in[i] || !out[i]) return MC_ERR_INVALID_ARG;
+            if (!aligned16(in[i]) || !aligned16(out[i]) || in[i] == out[i]) return MC_ERR_INVALID_ARG;
+        }
+    }
+    NsPlan P;
+    plan_ns(rows, cols, count, nullptr, P);
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < P.bytes) return MC_ERR_WORKSPACE;
+    plan_ns(rows, cols, count, (uint8_t*)ws, P);
+    mc_status st = run_mat_pass(P, step ? 0 : 1, w, g, m, in, rows, cols, 0, mu, lr, wd, rms_coef, nesterov, false,
+                                stream);
+    if (st != MC_OK) return st;
+    if ((st = run_norm(P, eps, stream)) != MC_OK) return st;
+    for (int it = 0; it < steps; ++it) {
+        if ((st = run_ns_phase(P, 0, it, a, b, c, stream)) != MC_OK) return st;
+        if ((st = run_ns_phase(P, 1, it, a, b, c, stream)) != MC_OK) return st;
+        if ((st = run_ns_phase(P, 2, it, a, b, c, stream)) != MC_OK) return st;
+    }
+    return run_mat_pass(P, step ? 2 : 3, step ? w : out, g, m, in, rows, cols, steps & 1, mu, lr, wd, rms_coef,
+                        nesterov, steps == 0, stream);
+}
+
+}  // namespace
+
+size_t mc_newton_schulz_workspace_size(const int* rows, const int* cols, int count) {
+    if (!valid_mats(rows, cols, count)) return 0;
+    NsPlan P;
+    plan_ns(rows, cols, count, nullptr, P);
+    return P.bytes;
+}
+
+size_t mc_muon_workspace_size(const int* rows, const int* cols, int count) {
+    return mc_newton_schulz_workspace_size(rows, cols, count);
+}
+
+mc_status mc_newton_schulz(const float* const* in, float* const* out, const int* rows, const int* cols, int count,
+                           int steps, float a, float b, float c, float eps, void* ws, size_t ws_bytes,
+                           mc_stream_t stream) {
+    return muon_impl(false, nullptr, nullptr, nullptr, in, out, rows, cols, count, 0.f, 0.f, 0.f, 0.f, steps, a, b,
+                     c, eps, 0, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+mc_status mc_muon_step(float* const* w, const float* const* g, float* const* m, const int* rows, const int* cols,
+                       int count, float lr, float mu, float wd, float rms_coef, int ns_steps, float a, float b,
+                       float c, float eps, int nesterov, void* ws, size_t ws_bytes, mc_stream_t stream) {
+    return muon_impl(true, w, g, m, nullptr, nullptr, rows, cols, count, lr, mu, wd, rms_coef, ns_steps, a, b, c,
+                     eps, nesterov, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+// ===========================================================================
+// tensor-core GEMM
+// ===========================================================================
+
+mc_status mc_gemm_bf16(const void* a, const void* b, void* c, mc_dtype c_type, int M, int N, int K, int batch,
+                       int b_kmajor, mc_stream_t stream) {
+    if (!a || !b || !c || M <= 0 || N <= 0 || K <= 0 || batch <= 0) return MC_ERR_INVALID_ARG;
+    if (c_type != MC_F32 && c_type != MC_BF16) return MC_ERR_INVALID_ARG;
+    if (K % 8 || (!b_kmajor && N % 8)) return MC_ERR_UNSUPPORTED;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(c)) return MC_ERR_INVALID_ARG;
+    GemmParams P;
+    memset(&P, 0, sizeof(P));
+    P.nprob = 1;
+    GemmProblem& q = P.p[0];
+    const uint64_t m = M, n = N, k = K, z = batch;
+    if (!make_tmap_3d(&q.tmA, a, k, m, z, k, m * k, kBK, kBM, 0)) return MC_ERR_INVALID_ARG;
+    if (b_kmajor) {
+        if (!make_tmap_3d(&q.tmB, b, k, n, z, k, n * k, kBK, kBN, 0)) return MC_ERR_INVALID_ARG;
+    } else {
+        if (!make_tmap_3d(&q.tmB, b, n, k, z, n, k * n, 64, kBK, 0)) return MC_ERR_INVALID_ARG;
+        q.b_mn = 1;
+    }
+    q.M = M;
+    q.N = N;
+    q.K = K;
+    q.batch = batch;
+    q.out_kind = c_type == MC_F32 ? kOutF32 : kOutBF16;
+    q.out = c;
+    q.out_ld = N;
+    q.out_bstride = (long long)M * N;
+    q.alpha = 1.f;
+    q.vec_ok = c_type == MC_F32 ? (N % 4 == 0) : (N % 8 == 0);
+    finalize_gemm_params(P);
+    MC_CUDA(launch_gemm(P, (cudaStream_t)stream, "gemm"));
+    return MC_OK;
+}
+
+}  // extern "C"

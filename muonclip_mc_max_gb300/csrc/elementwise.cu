@@ -1,0 +1,352 @@
+// elementwise.cu -- HBM-bound passes of the MuonClip step (sm_103a):
+//   * QK-Clip column-block scaling (MHA, MLA, global), one rounding per weight
+//   * Muon momentum + bf16 cast of the Newton-Schulz input (transposed for
+//     tall matrices) with a deterministic per-tile sum of squares
+//   * Frobenius-norm finalisation
+//   * the RMS-matched, weight-decayed update W <- W - lr (rms O + wd W)
+// All loads and stores are 128-bit where the layout allows.
+#include "common.cuh"
+#include "internal.h"
+
+namespace mc {
+
+// ---------------------------------------------------------------------------
+// QK-Clip
+// ---------------------------------------------------------------------------
+
+// gamma = min(1, tau / s), 1 when s is not > 0 (the K2 review's gamma
+// equation and its reference's where(before > 0, tau / before, 1)).
+MC_D float clip_gamma(float s, float tau) {
+    if (!(s > 0.0f)) return 1.0f;
+    return fminf(1.0f, __fdiv_rn(tau, s));
+}
+
+// Product w * f rounded to odd in float (Boldo & Melquiond, "Emulation of
+// FMA and correctly rounded sums: proved algorithms using rounding to odd",
+// 2008): p = RN(w f), e = w f - p exactly (fma); when e != 0 the result is
+// the truncation of w f with its last bit forced to 1.  A later RN to bf16
+// (8 < 24 - 1 bits) then equals one rounding of the exact product.
+MC_D float mul_round_odd(float w, float f) {
+    float p = __fmul_rn(w, f);
+    float e = __fmaf_rn(w, f, -p);
+    if (e != 0.0f) {
+        uint32_t u = __float_as_uint(p);
+        if ((e < 0.0f) != (p < 0.0f)) u -= 1u;  // |p| > |w f|: step toward zero
+        u |= 1u;
+        p = __uint_as_float(u);
+    }
+    return p;
+}
+
+MC_D void scale8_bf16(__nv_bfloat16* p, float f) {
+    uint4 u = *reinterpret_cast<const uint4*>(p);
+    __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(&u);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) h[i] = __float2bfloat16_rn(mul_round_odd(__bfloat162float(h[i]), f));
+    *reinterpret_cast<uint4*>(p) = u;
+}
+MC_D void scale8_f32(float* p, float f) {
+    float4 a = *reinterpret_cast<const float4*>(p);
+    float4 b = *reinterpret_cast<const float4*>(p + 4);
+    a.x = __fmul_rn(a.x, f); a.y = __fmul_rn(a.y, f); a.z = __fmul_rn(a.z, f); a.w = __fmul_rn(a.w, f);
+    b.x = __fmul_rn(b.x, f); b.y = __fmul_rn(b.y, f); b.z = __fmul_rn(b.z, f); b.w = __fmul_rn(b.w, f);
+    *reinterpret_cast<float4*>(p) = a;
+    *reinterpret_cast<float4*>(p + 4) = b;
+}
+
+// grid (H, nseg, chunks): block (h, s) scales head h's columns of segment s
+__global__ void clip_kernel(const ClipArgs a) {
+    const int h = blockIdx.x;
+    const ClipSeg& sg = a.seg[blockIdx.y];
+    const float g = clip_gamma(a.s_max[h], a.tau);
+    if (a.gamma_out && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0) a.gamma_out[h] = g;
+    if (g == 1.0f) return;  // unclipped head: never written
+    const float f = sg.use_gamma ? g : __fsqrt_rn(g);
+    const long long col = (long long)sg.col0 + (long long)h * sg.head_stride;
+    const bool vec = ((sg.ld | col | sg.width) & 7) == 0 && (reinterpret_cast<uintptr_t>(sg.w) & 15) == 0;
+    if (vec) {
+        const int per_row = sg.width >> 3;
+        const long long n = (long long)sg.rows * per_row;
+        for (long long i = (long long)blockIdx.z * blockDim.x + threadIdx.x; i < n;
+             i += (long long)gridDim.z * blockDim.x) {
+            long long r = i / per_row;
+            int v = (int)(i - r * per_row);
+            long long off = r * sg.ld + col + 8 * v;
+            if (a.bf16) scale8_bf16(reinterpret_cast<__nv_bfloat16*>(sg.w) + off, f);
+            else scale8_f32(reinterpret_cast<float*>(sg.w) + off, f);
+        }
+    } else {
+        const long long n = (long long)sg.rows * sg.width;
+        for (long long i = (long long)blockIdx.z * blockDim.x + threadIdx.x; i < n;
+             i += (long long)gridDim.z * blockDim.x) {
+            long long r = i / sg.width;
+            long long off = r * sg.ld + col + (i - r * sg.width);
+            if (a.bf16) {
+                __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(sg.w) + off;
+                *p = __float2bfloat16_rn(mul_round_odd(__bfloat162float(*p), f));
+            } else {
+                float* p = reinterpret_cast<float*>(sg.w) + off;
+                *p = __fmul_rn(*p, f);
+            }
+        }
+    }
+}
+
+cudaError_t launch_clip(const ClipArgs& a, cudaStream_t stream) {
+    if (a.H <= 0 || a.nseg <= 0) return cudaSuccess;
+    long long max_elems = 0;
+    for (int s = 0; s < a.nseg; ++s) {
+        long long e = (long long)a.seg[s].rows * a.seg[s].width;
+        if (e > max_elems) max_elems = e;
+    }
+    int threads = 256;
+    long long chunks = (max_elems / 8 + threads - 1) / threads;
+    if (chunks < 1) chunks = 1;
+    if (chunks > 64) chunks = 64;
+    dim3 grid(a.H, a.nseg, (unsigned)chunks);
+    TraceScope ts("clip", stream);
+    clip_kernel<<<grid, threads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+// Global clip: gamma from max_h s_max[h] (NaN propagates), then every
+// element of wq x gamma^alpha and of wk x gamma^(1-alpha).
+__global__ void clip_global_kernel(void* wq, void* wk, int bf16, long long n, const float* s_max, int H,
+                                   float tau, float alpha, float* gamma_out) {
+    float s = s_max[0];
+    for (int h = 1; h < H; ++h) s = max_nan(s, s_max[h]);
+    const float g = clip_gamma(s, tau);
+    if (gamma_out && blockIdx.x == 0 && threadIdx.x == 0) *gamma_out = g;
+    if (g == 1.0f) return;
+    const float fq = (float)pow((double)g, (double)alpha);
+    const float fk = (float)pow((double)g, 1.0 - (double)alpha);
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        if (bf16) {
+            __nv_bfloat16* q = reinterpret_cast<__nv_bfloat16*>(wq) + i;
+            __nv_bfloat16* k = reinterpret_cast<__nv_bfloat16*>(wk) + i;
+            *q = __float2bfloat16_rn(mul_round_odd(__bfloat162float(*q), fq));
+            *k = __float2bfloat16_rn(mul_round_odd(__bfloat162float(*k), fk));
+        } else {
+            float* q = reinterpret_cast<float*>(wq) + i;
+            float* k = reinterpret_cast<float*>(wk) + i;
+            *q = __fmul_rn(*q, fq);
+            *k = __fmul_rn(*k, fk);
+        }
+    }
+}
+
+cudaError_t launch_clip_global(void* wq, void* wk, int bf16, long long n, const float* s_max, int H, float tau,
+                               float alpha, float* gamma_out, cudaStream_t stream) {
+    int threads = 256;
+    long long blocks = (n + threads - 1) / threads;
+    if (blocks > 4096) blocks = 4096;
+    if (blocks < 1) blocks = 1;
+    TraceScope ts("clip_global", stream);
+    clip_global_kernel<<<(unsigned)blocks, threads, 0, stream>>>(wq, wk, bf16, n, s_max, H, tau, alpha,
+                                                                 gamma_out);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// bf16 -> fp16 (weights feeding an fp16 contraction)
+// ---------------------------------------------------------------------------
+__global__ void bf16_to_f16_kernel(const __nv_bfloat16* __restrict__ src, __half* __restrict__ dst, long long n) {
+    const long long nv = n / 8;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += (long long)gridDim.x * blockDim.x) {
+        uint4 u = reinterpret_cast<const uint4*>(src)[i];
+        const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+        uint4 o;
+        __half2* h = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) h[k] = __float22half2_rn(__bfloat1622float2(b[k]));
+        reinterpret_cast<uint4*>(dst)[i] = o;
+    }
+    for (long long i = nv * 8 + (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x)
+        dst[i] = __float2half_rn(__bfloat162float(src[i]));
+}
+
+cudaError_t launch_bf16_to_f16(const void* src, void* dst, long long n, cudaStream_t stream) {
+    if (n <= 0) return cudaSuccess;
+    int threads = 256;
+    long long blocks = (n / 8 + threads - 1) / threads;
+    if (blocks < 1) blocks = 1;
+    if (blocks > (long long)num_sms() * 8) blocks = (long long)num_sms() * 8;
+    TraceScope ts("to_f16", stream);
+    bf16_to_f16_kernel<<<(unsigned)blocks, threads, 0, stream>>>((const __nv_bfloat16*)src, (__half*)dst, n);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Muon passes over 64 x 64 tiles of X (the Newton-Schulz orientation)
+// ---------------------------------------------------------------------------
+constexpr int kTile = 64;
+constexpr int kMatThreads = 256;
+
+MC_D void find_mat(const MatBatch& B, int t, int& di) {
+    di = 0;
+    while (di + 1 < B.count && t >= B.d[di + 1].tile_begin) ++di;
+}
+
+// Source element (r, c) of the [rows][cols] matrix <-> X element (i, j):
+// X = S^T when tr, else X = S.
+__global__ void __launch_bounds__(kMatThreads) mat_pass_kernel(const __grid_constant__ MatBatch B) {
+    __shared__ float U[kTile][kTile + 1];
+    __shared__ double red[kMatThreads / 32];
+    const int tid = threadIdx.x;
+    for (int t = blockIdx.x; t < B.total_tiles; t += gridDim.x) {
+        int di;
+        find_mat(B, t, di);
+        const MatDesc& d = B.d[di];
+        const int local = t - d.tile_begin;
+        const int ti = local / d.tiles_x, tj = local - ti * d.tiles_x;
+        const int i0 = ti * kTile, j0 = tj * kTile;  // X tile origin
+        // the matching source tile: rows [sr0, sr0+64), cols [sc0, sc0+64)
+        const int sr0 = d.tr ? j0 : i0, sc0 = d.tr ? i0 : j0;
+        const int m = d.tr ? d.cols : d.rows, n = d.tr ? d.rows : d.cols;
+        const bool any = i0 < m && j0 < n;
+
+        if (B.mode <= 1) {
+            // ---- momentum (+ Nesterov) and cast: source -> U -> X ----
+            float ss = 0.f;
+            if (any) {
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    const int lr = p * 16 + (tid >> 4), lc = (tid & 15) * 4;
+                    const int r = sr0 + lr, c = sc0 + lc;
+                    float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (r < d.rows && c < d.cols) {
+                        const size_t off = (size_t)r * d.cols + c;
+                        float4 mv = *reinterpret_cast<const float4*>(d.m + off);
+                        if (B.mode == 0) {
+                            float4 gv = *reinterpret_cast<const float4*>(d.g + off);
+                            mv.x = __fmaf_rn(B.mu, mv.x, gv.x);
+                            mv.y = __fmaf_rn(B.mu, mv.y, gv.y);
+                            mv.z = __fmaf_rn(B.mu, mv.z, gv.z);
+                            mv.w = __fmaf_rn(B.mu, mv.w, gv.w);
+                            *reinterpret_cast<float4*>(d.m + off) = mv;
+                            if (B.nesterov) {
+                                u = make_float4(__fmaf_rn(B.mu, mv.x, gv.x), __fmaf_rn(B.mu, mv.y, gv.y),
+                                                __fmaf_rn(B.mu, mv.z, gv.z), __fmaf_rn(B.mu, mv.w, gv.w));
+                            } else {
+                                u = mv;
+                            }
+                        } else {
+                            u = mv;
+                        }
+                    }
+                    ss += u.x * u.x + u.y * u.y + u.z * u.z + u.w * u.w;
+                    U[lr][lc] = u.x;
+                    U[lr][lc + 1] = u.y;
+                    U[lr][lc + 2] = u.z;
+                    U[lr][lc + 3] = u.w;
+                }
+            }
+            __syncthreads();
+            // write X rows i0.., 4 consecutive j per thread (zeros in padding)
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const int li = p * 16 + (tid >> 4), lj = (tid & 15) * 4;
+                float v[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) v[k] = any ? (d.tr ? U[lj + k][li] : U[li][lj + k]) : 0.f;
+                __nv_bfloat162 h0 = __floats2bfloat162_rn(v[0], v[1]);
+                __nv_bfloat162 h1 = __floats2bfloat162_rn(v[2], v[3]);
+                uint2 pk;
+                pk.x = *reinterpret_cast<uint32_t*>(&h0);
+                pk.y = *reinterpret_cast<uint32_t*>(&h1);
+                *reinterpret_cast<uint2*>(d.x + (size_t)(i0 + li) * d.n_pad + j0 + lj) = pk;
+            }
+            // deterministic tile sum of squares
+            double s = (double)ss;
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+            if ((tid & 31) == 0) red[tid >> 5] = s;
+            __syncthreads();
+            if (tid == 0) {
+                double tot = 0.0;
+                for (int w = 0; w < kMatThreads / 32; ++w) tot += red[w];
+                d.partial[local] = tot;
+            }
+            __syncthreads();
+        } else {
+            // ---- X -> U -> update W (mode 2) or write O (mode 3) ----
+            if (!any) continue;
+            const float osc = d.oscale ? *d.oscale : 1.0f;
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const int li = p * 16 + (tid >> 4), lj = (tid & 15) * 4;
+                uint2 pk = *reinterpret_cast<const uint2*>(d.x + (size_t)(i0 + li) * d.n_pad + j0 + lj);
+                float2 a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&pk.x));
+                float2 b = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&pk.y));
+                U[li][lj] = a.x;
+                U[li][lj + 1] = a.y;
+                U[li][lj + 2] = b.x;
+                U[li][lj + 3] = b.y;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const int lr = p * 16 + (tid >> 4), lc = (tid & 15) * 4;
+                const int r = sr0 + lr, c = sc0 + lc;
+                if (r < d.rows && c < d.cols) {
+                    float o[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) o[k] = osc * (d.tr ? U[lc + k][lr] : U[lr][lc + k]);
+                    const size_t off = (size_t)r * d.cols + c;
+                    if (B.mode == 2) {
+                        float4 w = *reinterpret_cast<const float4*>(d.w + off);
+                        // W - lr (rms O + wd W), each step rounded as written
+                        w.x = w.x - B.lr * (d.rms * o[0] + B.wd * w.x);
+                        w.y = w.y - B.lr * (d.rms * o[1] + B.wd * w.y);
+                        w.z = w.z - B.lr * (d.rms * o[2] + B.wd * w.z);
+                        w.w = w.w - B.lr * (d.rms * o[3] + B.wd * w.w);
+                        *reinterpret_cast<float4*>(d.w + off) = w;
+                    } else {
+                        *reinterpret_cast<float4*>(d.w + off) = make_float4(o[0], o[1], o[2], o[3]);
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+cudaError_t launch_mat_pass(const MatBatch& b, cudaStream_t stream) {
+    if (b.total_tiles <= 0) return cudaSuccess;
+    int grid = num_sms() * 8;
+    if (grid > b.total_tiles) grid = b.total_tiles;
+    static const char* names[4] = {"muon_momentum", "ns_cast", "muon_update", "ns_out"};
+    TraceScope ts(names[b.mode & 3], stream);
+    mat_pass_kernel<<<grid, kMatThreads, 0, stream>>>(b);
+    return cudaGetLastError();
+}
+
+// s = 1 / (||U||_F + eps) from the tile partials, summed in a fixed order
+__global__ void norm_finalize_kernel(const __grid_constant__ NormArgs a) {
+    const int z = blockIdx.x;
+    if (z >= a.count) return;
+    __shared__ double red[256];
+    double s = 0.0;
+    for (int i = threadIdx.x; i < a.nparts[z]; i += blockDim.x) s += a.partial[z][i];
+    red[threadIdx.x] = s;
+    __syncthreads();
+    for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+        if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        double den = sqrt(red[0]) + (double)a.eps;
+        a.s[z] = (float)(1.0 / den);
+        a.s2[z] = (float)(1.0 / (den * den));
+    }
+}
+
+cudaError_t launch_norm_finalize(const NormArgs& a, cudaStream_t stream) {
+    if (a.count <= 0) return cudaSuccess;
+    TraceScope ts("norm_finalize", stream);
+    norm_finalize_kernel<<<a.count, 256, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace mc

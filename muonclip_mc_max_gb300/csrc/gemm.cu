@@ -1,0 +1,356 @@
+// gemm.cu -- persistent, warp-specialised tcgen05 GEMM for sm_103a.
+//
+// One CTA per SM walks a static round-robin list of 128 x 256 output tiles
+// drawn from up to four problems (projections of one layer, or one
+// Newton-Schulz phase over every matrix of a batch).
+//   warp 0      TMA producer: A tile 128 x 64 and B tile 256 x 64 (bf16,
+//               128-byte swizzle) per stage into a 4-stage ring
+//   warp 1      TMEM owner and MMA issuer: 4 x tcgen05.mma (K = 16) per
+//               stage into one of two 128 x 256 fp32 TMEM accumulators
+//   warps 2..5  epilogue: tcgen05.ld -> scale / aux / RoPE -> bf16 or f32
+//               global stores (mirrored for symmetric outputs)
+// The double-buffered accumulator lets the epilogue of tile t overlap the
+// MMAs of tile t+1.  Every wait is bounded (see mbar_wait).
+#include "common.cuh"
+#include "internal.h"
+
+namespace mc {
+
+constexpr int kAStageBytes = kBM * kBK * 2;  // 16 KB
+constexpr int kBStageBytes = kBN * kBK * 2;  // 32 KB
+constexpr int kGemmThreads = 192;
+constexpr int kGemmSmem = kGemmStages * (kAStageBytes + kBStageBytes) + 1024 + 256;
+
+struct GemmSmemTail {
+    uint64_t full[kGemmStages];
+    uint64_t empty[kGemmStages];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+MC_D void decode_tile(const GemmParams& P, int t, int& pi, int& z, int& tm, int& tn) {
+    pi = 0;
+    while (pi + 1 < P.nprob && t >= P.p[pi + 1].tile_begin) ++pi;
+    const GemmProblem& q = P.p[pi];
+    int local = t - q.tile_begin;
+    z = local / q.tiles_per_batch;
+    int r = local - z * q.tiles_per_batch;
+    if (!q.sym) {
+        tm = r / q.tiles_n;
+        tn = r - tm * q.tiles_n;
+    } else {
+        // row block tm holds the tiles tn >= tm/2 (those touching c >= r)
+        tm = 0;
+        while (true) {
+            int cnt = q.tiles_n - (tm >> 1);
+            if (r < cnt) {
+                tn = (tm >> 1) + r;
+                break;
+            }
+            r -= cnt;
+            ++tm;
+        }
+    }
+}
+
+MC_D void store_bf16x8(__nv_bfloat16* dst, const float* v) {
+    __nv_bfloat162 h[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<uint4*>(h);
+}
+MC_D void store_f16x8(__half* dst, const float* v) {
+    __half2 h[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<uint4*>(h);
+}
+
+// Epilogue for 64 consecutive columns [col0, col0 + 64) of row r.
+MC_D void epilogue_chunk(const GemmProblem& q, int z, int r, int col0, float* f, float sc, unsigned* status) {
+    if (r >= q.M || col0 >= q.N) return;
+    if (q.rope_tab && (col0 % q.rope_period) == q.rope_start) {
+        const float2* cs = q.rope_tab + (size_t)(r % q.rope_T) * 32;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            float2 t = cs[i];
+            float lo = f[i], hi = f[i + 32];
+            f[i] = lo * t.x - hi * t.y;
+            f[i + 32] = hi * t.x + lo * t.y;
+        }
+    }
+    if (q.aux) {
+        const __nv_bfloat16* ap = q.aux + (size_t)z * q.aux_bstride + (size_t)r * q.aux_ld + col0;
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+            uint4 u = *reinterpret_cast<const uint4*>(ap + 8 * v);
+            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float2 a2 = __bfloat1622float2(h[i]);
+                f[8 * v + 2 * i] = sc * (q.alpha * f[8 * v + 2 * i] + q.beta * a2.x);
+                f[8 * v + 2 * i + 1] = sc * (q.alpha * f[8 * v + 2 * i + 1] + q.beta * a2.y);
+            }
+        }
+    } else if (q.alpha != 1.0f || sc != 1.0f) {
+        float s = sc * q.alpha;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) f[i] *= s;
+    }
+    if (q.out_kind == kOutF16) {
+        __half* o = reinterpret_cast<__half*>(q.out) + (size_t)z * q.out_bstride + (size_t)r * q.out_ld;
+        bool big = false;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) big |= fabsf(f[i]) > 65504.0f;
+        if (big) set_status(status, MC_DEV_RANGE);
+        if (q.vec_ok && col0 + 64 <= q.N) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v) store_f16x8(o + col0 + 8 * v, f + 8 * v);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 64; ++i)
+                if (col0 + i < q.N) o[col0 + i] = __float2half_rn(f[i]);
+        }
+        return;
+    }
+    if (q.out_kind == kOutF32) {
+        float* o = reinterpret_cast<float*>(q.out) + (size_t)z * q.out_bstride + (size_t)r * q.out_ld;
+        if (q.vec_ok && col0 + 64 <= q.N) {
+#pragma unroll
+            for (int v = 0; v < 16; ++v)
+                *reinterpret_cast<float4*>(o + col0 + 4 * v) =
+                    make_float4(f[4 * v], f[4 * v + 1], f[4 * v + 2], f[4 * v + 3]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 64; ++i)
+                if (col0 + i < q.N) o[col0 + i] = f[i];
+        }
+        return;
+    }
+    __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(q.out) + (size_t)z * q.out_bstride;
+    if (!q.sym) {
+        __nv_bfloat16* o = ob + (size_t)r * q.out_ld;
+        if (q.vec_ok && col0 + 64 <= q.N) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v) store_bf16x8(o + col0 + 8 * v, f + 8 * v);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 64; ++i)
+                if (col0 + i < q.N) o[col0 + i] = __float2bfloat16_rn(f[i]);
+        }
+        return;
+    }
+    // symmetric: keep c >= r, mirror to (c, r).  Lanes hold consecutive rows,
+    // so the mirrored stores of one column are coalesced across the warp.
+    if (q.vec_ok && col0 >= r && col0 + 64 <= q.N) {
+        __nv_bfloat16* o = ob + (size_t)r * q.out_ld;
+#pragma unroll
+        for (int v = 0; v < 8; ++v) store_bf16x8(o + col0 + 8 * v, f + 8 * v);
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+            ob[(size_t)(col0 + i) * q.out_ld + r] = __float2bfloat16_rn(f[i]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+            int c = col0 + i;
+            if (c >= r && c < q.N) {
+                __nv_bfloat16 h = __float2bfloat16_rn(f[i]);
+                ob[(size_t)r * q.out_ld + c] = h;
+                ob[(size_t)c * q.out_ld + r] = h;
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParams P) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + kGemmStages * kAStageBytes;
+    GemmSmemTail* tail = reinterpret_cast<GemmSmemTail*>(sB + kGemmStages * kBStageBytes);
+    volatile int* abort_flag = &tail->abort_flag;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kGemmStages; ++s) {
+            mbar_init(&tail->full[s], 1);
+            mbar_init(&tail->empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tail->tfull[a], 1);
+            mbar_init(&tail->tempty[a], 4);
+        }
+        mbar_init(&tail->drain, 1);
+        tail->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        for (int i = 0; i < P.nprob; ++i) {
+            tma_prefetch_desc(&P.p[i].tmA);
+            tma_prefetch_desc(&P.p[i].tmB);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(&tail->tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = tail->tmem_base;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued[kGemmStages] = {0, 0, 0, 0};
+            bool ok = true;
+            for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
+                int pi, z, tm, tn;
+                decode_tile(P, t, pi, z, tm, tn);
+                const GemmProblem& q = P.p[pi];
+                const int nk = (q.K + kBK - 1) / kBK;
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(&tail->empty[stage], phase ^ 1, abort_flag, P.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&tail->full[stage], kAStageBytes + kBStageBytes);
+                    tma_load_3d(sA + stage * kAStageBytes, &q.tmA, &tail->full[stage], kb * kBK,
+                                tm * kBM, z);
+                    uint8_t* b = sB + stage * kBStageBytes;
+                    if (!q.b_mn) {
+                        tma_load_3d(b, &q.tmB, &tail->full[stage], kb * kBK, tn * kBN, z);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            tma_load_3d(b + j * (kBK * 128), &q.tmB, &tail->full[stage],
+                                        tn * kBN + j * 64, kb * kBK, z);
+                    }
+                    ++issued[stage];
+                    if (++stage == kGemmStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            // wait for this thread's copies still in flight before exit
+            for (int s = 0; s < kGemmStages; ++s)
+                if (issued[s]) {
+                    volatile int never = 0;
+                    mbar_wait(&tail->full[s], (issued[s] - 1) & 1, &never, P.status);
+                }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        int stage = 0, acc = 0;
+        uint32_t phase = 0, aphase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
+            int pi, z, tm, tn;
+            decode_tile(P, t, pi, z, tm, tn);
+            const GemmProblem& q = P.p[pi];
+            const int nk = (q.K + kBK - 1) / kBK;
+            const uint32_t idesc = idesc_f16kind(kBM, kBN, q.b_mn, q.ab_f16);
+            if (!mbar_wait(&tail->tempty[acc], aphase ^ 1, abort_flag, P.status)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
+            for (int kb = 0; kb < nk; ++kb) {
+                if (!mbar_wait(&tail->full[stage], phase, abort_flag, P.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t a0 = smem_u32(sA + stage * kAStageBytes);
+                    const uint32_t b0 = smem_u32(sB + stage * kBStageBytes);
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k) {
+                        uint64_t ad = sw128_desc(a0 + k * 32, 16, 1024);
+                        uint64_t bd = q.b_mn ? sw128_desc(b0 + k * 2048, kBK * 128, 1024)
+                                             : sw128_desc(b0 + k * 32, 16, 1024);
+                        umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0);
+                    }
+                    umma_commit(&tail->empty[stage]);
+                }
+                __syncwarp();
+                if (++stage == kGemmStages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (!ok) break;
+            if (lane == 0) umma_commit(&tail->tfull[acc]);
+            __syncwarp();
+            if (++acc == 2) {
+                acc = 0;
+                aphase ^= 1;
+            }
+        }
+        // drain: every MMA this thread issued has completed before teardown
+        if (lane == 0) umma_commit(&tail->drain);
+        __syncwarp();
+        volatile int never = 0;
+        mbar_wait(&tail->drain, 0, &never, P.status);
+    } else {
+        // ---------------- epilogue (warps 2..5) ----------------
+        const int quarter = warp & 3;  // TMEM lanes this warp may access
+        int acc = 0;
+        uint32_t aphase = 0;
+        for (int t = blockIdx.x; t < P.total_tiles; t += gridDim.x) {
+            int pi, z, tm, tn;
+            decode_tile(P, t, pi, z, tm, tn);
+            const GemmProblem& q = P.p[pi];
+            if (!mbar_wait(&tail->tfull[acc], aphase, abort_flag, P.status)) break;
+            tc_fence_after();
+            const int r = tm * kBM + quarter * 32 + lane;
+            const float sc = q.scale ? q.scale[z] : 1.0f;
+#pragma unroll 1
+            for (int c = 0; c < kBN / 64; ++c) {
+                uint32_t v[64];
+                uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN + c * 64);
+                tmem_ld32(taddr, v);
+                tmem_ld32(taddr + 32, v + 32);
+                tmem_ld_wait();
+                epilogue_chunk(q, z, r, tn * kBN + c * 64, reinterpret_cast<float*>(v), sc, P.status);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tail->tempty[acc]);
+            if (++acc == 2) {
+                acc = 0;
+                aphase ^= 1;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, 512);
+}
+
+cudaError_t launch_gemm(const GemmParams& P, cudaStream_t stream, const char* label) {
+    if (P.total_tiles <= 0) return cudaSuccess;
+    static bool attr_set[64] = {false};
+    int dev = current_device();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    if (dev < 64 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    int grid = num_sms();
+    if (grid > P.total_tiles) grid = P.total_tiles;
+    TraceScope ts(label, stream);
+    gemm_kernel<<<grid, kGemmThreads, kGemmSmem, stream>>>(P);
+    return cudaGetLastError();
+}
+
+}  // namespace mc

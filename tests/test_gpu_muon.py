@@ -1,0 +1,102 @@
+"""Newton-Schulz and Muon-step parity against the fp64 oracle: relative
+Frobenius error <= 2e-2 for the orthogonalised update (bf16 operands, fp32
+accumulation), momentum to fp32 rounding, weights bit-unchanged at lr = 0."""
+import numpy as np
+import pytest
+import torch
+
+import mc_inputs
+import oracle
+from gpu_helpers import NS_RTOL, dev, lib, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("shape", [(64, 32), (32, 64), (256, 256), (200, 520), (520, 200),
+                                   (1024, 1024), (576, 1024)])
+def test_newton_schulz_vs_oracle(shape):
+    lib()
+    from muonclip_mc_max_gb300 import api
+    g = mc_inputs.matrix(*shape, seed=shape[0] * 3 + shape[1])
+    out = api.mc_newton_schulz([g.to(dev())])[0]
+    torch.cuda.synchronize()
+    ref = oracle.newton_schulz(g)
+    assert rel_fro(out.cpu().numpy(), ref) < NS_RTOL
+
+
+def test_newton_schulz_mixed_batch():
+    """Several shapes in one call (grouped by padded shape, one launch per
+    phase)."""
+    lib()
+    from muonclip_mc_max_gb300 import api
+    shapes = [(64, 32), (300, 128), (128, 300), (256, 512), (512, 256), (96, 96)]
+    mats = [mc_inputs.matrix(r, c, seed=100 + i) for i, (r, c) in enumerate(shapes)]
+    outs = api.mc_newton_schulz([m.to(dev()) for m in mats])
+    torch.cuda.synchronize()
+    for m, o in zip(mats, outs):
+        assert rel_fro(o.cpu().numpy(), oracle.newton_schulz(m)) < NS_RTOL
+
+
+@pytest.mark.parametrize("steps", [0, 1, 5])
+def test_newton_schulz_steps(steps):
+    lib()
+    from muonclip_mc_max_gb300 import api
+    g = mc_inputs.matrix(128, 384, seed=7)
+    out = api.mc_newton_schulz([g.to(dev())], steps=steps)[0]
+    torch.cuda.synchronize()
+    assert rel_fro(out.cpu().numpy(), oracle.newton_schulz(g, steps)) < NS_RTOL
+
+
+@pytest.mark.parametrize("nesterov", [False, True])
+def test_c1_muon_step(nesterov):
+    """The tiny workload: 64 x 32 momentum, lr 2e-4, wd 0.1, RMS 0.2."""
+    lib()
+    from muonclip_mc_max_gb300 import api
+    inp = mc_inputs.c1()
+    w, g, m = inp["w"], inp["grad"], inp["m_prev"]
+    wd_, gd, md = w.to(dev()), g.to(dev()), m.to(dev())
+    api.mc_muon_step([wd_], [gd], [md], lr=2e-4, mu=0.95, wd=0.1, rms=0.2, nesterov=nesterov)
+    torch.cuda.synchronize()
+    rw, rm, ro = oracle.muon_step(w, g, m, lr=2e-4, mu=0.95, wd=0.1, rms=0.2, nesterov=nesterov)
+    assert rel_fro(md.cpu().numpy(), rm) < 1e-6
+    upd = (wd_.cpu().double().numpy() - w.double().numpy())
+    assert rel_fro(upd, rw - w.double().numpy()) < NS_RTOL
+    assert rel_fro(wd_.cpu().numpy(), rw) < 1e-5
+
+
+def test_muon_batch_mixed_and_resume():
+    lib()
+    from muonclip_mc_max_gb300 import api
+    shapes = [(256, 128), (128, 256), (384, 384)]
+    W = [mc_inputs.matrix(r, c, seed=200 + i, std=0.006) for i, (r, c) in enumerate(shapes)]
+    G1 = [mc_inputs.matrix(r, c, seed=300 + i, std=1e-3) for i, (r, c) in enumerate(shapes)]
+    G2 = [mc_inputs.matrix(r, c, seed=400 + i, std=1e-3) for i, (r, c) in enumerate(shapes)]
+    M = [mc_inputs.matrix(r, c, seed=500 + i, std=1e-3) for i, (r, c) in enumerate(shapes)]
+    wd_ = [t.to(dev()) for t in W]
+    md = [t.to(dev()) for t in M]
+    api.mc_muon_step(wd_, [t.to(dev()) for t in G1], md, lr=2e-4)
+    # save, reload, second step == continuing (the library keeps no state)
+    saved_w = [t.clone() for t in wd_]
+    saved_m = [t.clone() for t in md]
+    api.mc_muon_step(wd_, [t.to(dev()) for t in G2], md, lr=2e-4)
+    api.mc_muon_step(saved_w, [t.to(dev()) for t in G2], saved_m, lr=2e-4)
+    torch.cuda.synchronize()
+    for a, b in zip(wd_ + md, saved_w + saved_m):
+        assert torch.equal(a, b)
+    for i in range(3):
+        rw, rm, _ = oracle.muon_step(W[i], G1[i], M[i], lr=2e-4)
+        rw, rm, _ = oracle.muon_step(rw, G2[i], rm, lr=2e-4)
+        assert rel_fro(md[i].cpu().numpy(), rm) < 1e-6
+        assert rel_fro(wd_[i].cpu().double().numpy() - W[i].double().numpy(),
+                       rw - W[i].double().numpy()) < NS_RTOL
+
+
+def test_lr_zero_leaves_weights_bit_unchanged():
+    lib()
+    from muonclip_mc_max_gb300 import api
+    w = mc_inputs.matrix(128, 256, seed=9)
+    wd_ = w.to(dev())
+    api.mc_muon_step([wd_], [mc_inputs.matrix(128, 256, seed=10).to(dev())],
+                     [torch.zeros(128, 256, device=dev())], lr=0.0)
+    torch.cuda.synchronize()
+    assert torch.equal(wd_.cpu(), w)
