@@ -80,6 +80,9 @@ class Workload:
     def step(self, s, api):
         raise NotImplementedError
 
+    def step_part(self, s, api, part):
+        raise NotImplementedError
+
 
 class MhaLayer(Workload):
     """c2: MHA layer + Muon on the W_q / W_k masters + clip."""
@@ -96,15 +99,15 @@ class MhaLayer(Workload):
         self.units = {
             "gemm:proj": ("tensor", 2 * 2 * B * T * D * N),
             "scan": ("tensor", 2 * scan_pairs(B, T, False) * H * dh),
-            "gemm:ns_gram": ("tensor", 2 * ns["gram"]),
-            "gemm:ns_poly": ("tensor", 2 * ns["poly"]),
-            "gemm:ns_apply": ("tensor", 2 * ns["apply"]),
+            "gemm:ns_gram": ("tensor", 5 * 2 * ns["gram"]),
+            "gemm:ns_poly": ("tensor", 5 * 2 * ns["poly"]),
+            "gemm:ns_apply": ("tensor", 5 * 2 * ns["apply"]),
             "muon_momentum": ("hbm", 2 * D * N * 14),
             "muon_update": ("hbm", 2 * D * N * 10),
         }
         self.scan_flops = self.units["gemm:proj"][1] + self.units["scan"][1]
-        self.ns_flops = 5 * sum(self.units[k][1] for k in ("gemm:ns_gram", "gemm:ns_poly",
-                                                          "gemm:ns_apply"))
+        self.ns_flops = sum(self.units[k][1] for k in ("gemm:ns_gram", "gemm:ns_poly",
+                                                      "gemm:ns_apply"))
 
     def make(self, device):
         inp = mc_inputs.c2(device=device, B=self.B, T=self.T, D=self.D, H=self.H, dh=self.dh)
@@ -123,16 +126,20 @@ class MhaLayer(Workload):
     def outputs(self, s):
         return [s["s_max"], s["gamma"]]
 
-    def step(self, s, api, marks=None):
-        api.mc_max_logits_mha(s["x"], s["wq"], s["wk"], self.H, self.dh, s_max=s["s_max"])
-        if marks:
-            marks[0].record()
-        api.mc_muon_step(s["masters"], s["grad"], s["moms"], lr=mc_inputs.LR, mu=mc_inputs.MU,
-                         wd=mc_inputs.WD, rms=mc_inputs.RMS, steps=mc_inputs.NS_STEPS)
-        if marks:
-            marks[1].record()
-        api.mc_qk_clip_mha(s["masters"][0], s["masters"][1], self.H, self.dh, s["s_max"],
-                           s["tau"], gamma=s["gamma"])
+    def step(self, s, api):
+        self.step_part(s, api, "scan")
+        self.step_part(s, api, "muon")
+        self.step_part(s, api, "clip")
+
+    def step_part(self, s, api, part):
+        if part == "scan":
+            api.mc_max_logits_mha(s["x"], s["wq"], s["wk"], self.H, self.dh, s_max=s["s_max"])
+        elif part == "muon":
+            api.mc_muon_step(s["masters"], s["grad"], s["moms"], lr=mc_inputs.LR, mu=mc_inputs.MU,
+                             wd=mc_inputs.WD, rms=mc_inputs.RMS, steps=mc_inputs.NS_STEPS)
+        else:
+            api.mc_qk_clip_mha(s["masters"][0], s["masters"][1], self.H, self.dh, s["s_max"],
+                               s["tau"], gamma=s["gamma"])
 
     # --- oracle sample for the CPU baseline ---------------------------------
     def oracle_sample(self, s):
@@ -148,7 +155,7 @@ class MhaLayer(Workload):
         N = self.H * self.dh
         m, n = min(self.D, N), max(self.D, N)
         flops = len(heads) * (2 * 2 * self.T * self.D * self.dh + 2 * self.T * self.T * self.dh)
-        flops += 5 * sum(2 * v for v in ns_flops_per_iter(m, n).values())
+        flops += 5 * sum(ns_flops_per_iter(m, n).values())
         return flops, dt, (f"2 of {self.B * self.H} (sequence, head) scans and 1 of 2 "
                            f"Muon steps ({self.D}x{N}), fp64")
 
@@ -164,15 +171,15 @@ class ExpertBatch(Workload):
         ns = ns_flops_per_iter(2048, 7168)
         cnt = n_up + n_down
         self.units = {
-            "gemm:ns_gram": ("tensor", 2 * ns["gram"] * cnt),
-            "gemm:ns_poly": ("tensor", 2 * ns["poly"] * cnt),
-            "gemm:ns_apply": ("tensor", 2 * ns["apply"] * cnt),
+            "gemm:ns_gram": ("tensor", 5 * ns["gram"] * cnt),
+            "gemm:ns_poly": ("tensor", 5 * ns["poly"] * cnt),
+            "gemm:ns_apply": ("tensor", 5 * ns["apply"] * cnt),
             "muon_momentum": ("hbm", cnt * 2048 * 7168 * 14),
             "muon_update": ("hbm", cnt * 2048 * 7168 * 10),
         }
         self.scan_flops = 0
-        self.ns_flops = 5 * (self.units["gemm:ns_gram"][1] + self.units["gemm:ns_poly"][1]
-                             + self.units["gemm:ns_apply"][1])
+        self.ns_flops = (self.units["gemm:ns_gram"][1] + self.units["gemm:ns_poly"][1]
+                         + self.units["gemm:ns_apply"][1])
 
     def make(self, device):
         return mc_inputs.c4(device=device, n_up=self.n_up, n_down=self.n_down)
@@ -183,12 +190,12 @@ class ExpertBatch(Workload):
     def outputs(self, s):
         return []
 
-    def step(self, s, api, marks=None):
-        if marks:
-            marks[0].record()
-        api.mc_muon_step(s["w"], s["grad"], s["m_prev"], lr=mc_inputs.LR)
-        if marks:
-            marks[1].record()
+    def step(self, s, api):
+        self.step_part(s, api, "muon")
+
+    def step_part(self, s, api, part):
+        if part == "muon":
+            api.mc_muon_step(s["w"], s["grad"], s["m_prev"], lr=mc_inputs.LR)
 
     def oracle_sample(self, s):
         import oracle
@@ -196,7 +203,7 @@ class ExpertBatch(Workload):
         oracle.newton_schulz(s["m_prev"][0][:512].cpu(), 5)
         dt = time.perf_counter() - t0
         m, n = 512, 2048
-        flops = 5 * sum(2 * v for v in ns_flops_per_iter(m, n).values())
+        flops = 5 * sum(ns_flops_per_iter(m, n).values())
         return flops, dt, "Newton-Schulz of one 512x2048 slice of an expert momentum, fp64"
 
 
@@ -214,14 +221,14 @@ class MlaLayer(Workload):
                      + ("; Muon on W_qa, W_qb, W_kva, W_kb; MLA clip" if self.muon else ""))
         BT = self.B * self.T
         proj = 2 * BT * (7168 * 1536 + 7168 * 576 + 1536 * 64 * 192 + 512 * 64 * 128)
-        self.units = {"gemm:proj": ("tensor", proj / 2),  # two launches per step
+        self.units = {"gemm:proj": ("tensor", proj),
                       "scan": ("tensor", 2 * scan_pairs(self.B, self.T, True) * 64 * 192)}
         self.scan_flops = proj + self.units["scan"][1]
         self.ns_flops = 0
         if self.muon:
             for r, c in [(7168, 1536), (1536, 12288), (7168, 576), (512, 8192)]:
                 m, n = min(r, c), max(r, c)
-                self.ns_flops += 5 * sum(2 * v for v in ns_flops_per_iter(m, n).values())
+                self.ns_flops += 5 * sum(ns_flops_per_iter(m, n).values())
 
     def make(self, device):
         fn = mc_inputs.c5 if self.which == "c5" else mc_inputs.c3
@@ -241,15 +248,20 @@ class MlaLayer(Workload):
     def outputs(self, s):
         return [s["s_max"], s["gamma"]]
 
-    def step(self, s, api, marks=None):
-        api.mc_max_logits_mla(s["x"], s["w_qa"], s["w_qb"], s["w_kva"], s["w_kb"], 64, 128, 64,
-                              s["rope_base"], causal=True, s_max=s["s_max"])
-        if marks:
-            marks[0].record()
-        if self.muon:
-            api.mc_muon_step(s["masters"], s["grad"], s["moms"], lr=mc_inputs.LR)
-        if marks:
-            marks[1].record()
+    def step(self, s, api):
+        self.step_part(s, api, "scan")
+        self.step_part(s, api, "muon")
+        self.step_part(s, api, "clip")
+
+    def step_part(self, s, api, part):
+        if part == "scan":
+            api.mc_max_logits_mla(s["x"], s["w_qa"], s["w_qb"], s["w_kva"], s["w_kb"], 64, 128, 64,
+                                  s["rope_base"], causal=True, s_max=s["s_max"])
+            return
+        if part == "muon":
+            if self.muon:
+                api.mc_muon_step(s["masters"], s["grad"], s["moms"], lr=mc_inputs.LR)
+            return
         if self.muon:
             api.mc_qk_clip_mla(s["masters"][1], s["masters"][3], 64, 128, 64, s["s_max"], s["tau"],
                                gamma=s["gamma"])
@@ -394,31 +406,35 @@ def run_ours(args, wl):
         if world > 1:
             dist.barrier()
 
+    from muonclip_mc_max_gb300.step import CapturedStep
+
+    # the whole step as one CUDA graph (launch-bound at small sizes); the
+    # scan and Muon halves are also captured alone for the breakdown
+    n0 = api.mc_launch_count()
+    graph = CapturedStep(lambda: wl.step(s, api), warmup=2)
+    per_step_launches = (api.mc_launch_count() - n0) // 3  # 2 warm-up runs + the capture
+    g_scan = CapturedStep(lambda: wl.step_part(s, api, "scan"), warmup=1) if wl.scan_flops else None
+    g_muon = CapturedStep(lambda: wl.step_part(s, api, "muon"), warmup=1) if wl.ns_flops else None
     for _ in range(max(args.warmup, 3)):
-        wl.step(s, api)
+        graph.replay()
     assert api.mc_read_device_status(clear=True) == 0, "device status set during warm-up"
 
     # ---- timed region: device time per step, L2 flushed between steps ----
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
     clocks = ClockSampler(local)
     clocks.start()
     barrier()
-    launches0 = api.mc_launch_count()
     for k in range(K):
         flush.zero_()
-        e0, m0, m1, e1 = ev[k]
-        e0.record(stream)
-        wl.step(s, api, marks=(m0, m1))
-        e1.record(stream)
+        ev[k][0].record(stream)
+        graph.replay()
+        ev[k][1].record(stream)
     barrier()
-    launches = api.mc_launch_count() - launches0
     clk = clocks.stop()
-    step_ms = [a.elapsed_time(b) for a, _, _, b in ev]
-    scan_ms = [a.elapsed_time(m) for a, m, _, _ in ev]
-    muon_ms = [m.elapsed_time(n) for _, m, n, _ in ev]
+    launches = per_step_launches * K
+    step_ms = [a.elapsed_time(b) for a, b in ev]
     tot_ms = sum(step_ms)
     if world > 1:
         t = torch.tensor([tot_ms], device=device)
@@ -429,44 +445,67 @@ def run_ours(args, wl):
     value = world * flops / (ms * 1e-3) / 1e12
     hbm_peak, bf16_peak, bf16_sus, peak_src = load_peaks()
 
-    # ---- per-kernel event times (separate pass, same steps) ----
+    def part_ms(g):
+        if g is None:
+            return None
+        e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(K)]
+        for k in range(K):
+            flush.zero_()
+            e[k][0].record(stream)
+            g.replay()
+            e[k][1].record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in e)
+
+    scan_t, muon_t = part_ms(g_scan), part_ms(g_muon)
+
+    # ---- per-kernel times: a graph captured with event nodes around every
+    # launch (on the launching stream), read back after each replay ----
+    api.mc_trace_collect()  # drop anything recorded so far
     api.mc_trace_enable(True)
+    traced = CapturedStep(lambda: wl.step(s, api), warmup=0)
+    api.mc_trace_enable(False)
+    trace = {}
     for k in range(K):
         flush.zero_()
-        wl.step(s, api)
-    torch.cuda.synchronize()
-    api.mc_trace_enable(False)
-    trace = api.mc_trace_collect()
+        traced.replay()
+        torch.cuda.synchronize()
+        for name, (n, tms) in api.mc_trace_collect(keep=True).items():
+            a = trace.setdefault(name, [0, 0.0])
+            a[0] += n
+            a[1] += tms
+    api.mc_trace_collect(keep=False)
     kernels = {}
-    for name, (n, tms) in trace.items():
-        entry = {"launches_per_step": n / K, "ms_per_launch": tms / n,
-                 "share": None}
-        if name in wl.units:
-            kind, work = wl.units[name]
-            if kind == "tensor":
-                entry["achieved_tflops"] = work / (tms / n * 1e-3) / 1e12
-            else:
-                entry["achieved_gbs"] = work / (tms / n * 1e-3) / 1e9
-        kernels[name] = entry
     tot_k = sum(v[1] for v in trace.values()) or 1.0
     for name, (n, tms) in trace.items():
-        kernels[name]["share"] = tms / tot_k
+        entry = {"launches_per_step": n / K, "ms_per_launch": tms / n, "ms_per_step": tms / K,
+                 "share": tms / tot_k}
+        if name in wl.units:
+            kind, work = wl.units[name]  # algorithmic work per step
+            if kind == "tensor":
+                entry["achieved_tflops"] = work / (tms / K * 1e-3) / 1e12
+            else:
+                entry["achieved_gbs"] = work / (tms / K * 1e-3) / 1e9
+        kernels[name] = entry
     dominant = max((k for k in kernels if k in wl.units), key=lambda k: trace[k][1])
     kind, work = wl.units[dominant]
-    dur = trace[dominant][1] / trace[dominant][0] * 1e-3
+    n_launch = trace[dominant][0] / K
+    dur = trace[dominant][1] / trace[dominant][0] * 1e-3      # s per launch
     if kind == "tensor":
-        achieved = work / dur / 1e12
+        achieved = work / n_launch / dur / 1e12
         roof = {"kernel": dominant, "bound": "tensor", "achieved": achieved, "peak": bf16_peak,
                 "unit": "TFLOP/s", "frac": achieved / bf16_peak, "traffic": None,
                 "peak_kind": f"{peak_src} bf16 dense (burst)"}
     else:
-        achieved = work / dur / 1e9
+        achieved = work / n_launch / dur / 1e9
         roof = {"kernel": dominant, "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
                 "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": None,
                 "peak_kind": f"{peak_src} HBM copy"}
     assert api.mc_read_device_status(clear=True) == 0, "device status set during timing"
 
-    # ---- end to end through the public API (pinned H2D inputs, D2H results) ----
+    # ---- end to end through the public API: pinned H2D of the step's inputs,
+    # the captured step, D2H of its results ----
     ins = wl.inputs(s)
     outs = wl.outputs(s)
     host_in = [t.detach().cpu().pin_memory() for t in ins]
@@ -478,7 +517,7 @@ def run_ours(args, wl):
     for k in range(K):
         for hd, dv in zip(host_in, ins):
             dv.copy_(hd, non_blocking=True)
-        wl.step(s, api)
+        graph.replay()
         for hd, dv in zip(host_out, outs):
             hd.copy_(dv, non_blocking=True)
         stream.synchronize()
@@ -502,8 +541,6 @@ def run_ours(args, wl):
         cpu = {"value": f_tot / dt_tot / 1e12, "unit": "TFLOP/s",
                "cores": int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)),
                "kind": "oracle", "sample": f"{sample}; {reps} repetitions, {dt_tot:.1f} s"}
-        scan_t = statistics.mean(scan_ms)
-        muon_t = statistics.mean(muon_ms)
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": ms,
@@ -512,12 +549,12 @@ def run_ours(args, wl):
             "config": {"workload": wl.desc, "l2": "flushed between timed steps (256 MiB write)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "muonclip_step_ms": ms,
-            "scan_tflops": (wl.scan_flops / (scan_t * 1e-3) / 1e12) if wl.scan_flops else None,
+            "scan_tflops": (wl.scan_flops / (scan_t * 1e-3) / 1e12) if scan_t else None,
             "scan_frac_bf16_peak": ((wl.scan_flops / (scan_t * 1e-3) / 1e12) / bf16_peak)
-            if wl.scan_flops else None,
-            "ns_tflops": (wl.ns_flops / (muon_t * 1e-3) / 1e12) if wl.ns_flops else None,
+            if scan_t else None,
+            "ns_tflops": (wl.ns_flops / (muon_t * 1e-3) / 1e12) if muon_t else None,
             "ns_frac_bf16_peak": ((wl.ns_flops / (muon_t * 1e-3) / 1e12) / bf16_peak)
-            if wl.ns_flops else None,
+            if muon_t else None,
             "scan_ms": scan_t, "muon_ms": muon_t,
             "roofline": roof,
             "kernels": kernels,
@@ -540,8 +577,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c2")
+    ap.add_argument("--experts", type=int, default=48,
+                    help="c4: up- and down-projections each (smaller for profiling)")
     args = ap.parse_args()
-    wl = WORKLOADS[args.workload]()
+    wl = (ExpertBatch(args.experts, args.experts) if args.workload == "c4"
+          else WORKLOADS[args.workload]())
     if args.impl == "reference":
         run_reference(args, wl)
     else:

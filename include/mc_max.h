@@ -249,10 +249,13 @@ typedef struct mc_trace_entry {
     double total_ms;     /* sum of their event-measured durations      */
 } mc_trace_entry;
 
-/* Synchronises on the recorded events, aggregates them per kernel kind into
- * out[0..cap) and forgets them.  Returns the number of kinds (may exceed
- * cap; only cap are written), or -1 on a CUDA error. */
-int mc_trace_collect(mc_trace_entry* out, int cap);
+/* Synchronises on the recorded events and aggregates them per kernel kind
+ * into out[0..cap).  keep == 0 forgets the records afterwards; keep != 0
+ * leaves them, so launches captured into a CUDA graph (whose event-record
+ * nodes re-record the same events on every replay) can be read after each
+ * replay.  Returns the number of kinds (may exceed cap; only cap are
+ * written), or -1 on a CUDA error. */
+int mc_trace_collect(mc_trace_entry* out, int cap, int keep);
 
 #ifdef __cplusplus
 }

@@ -5,6 +5,6 @@ ctypes binding.  See ``api`` for the functions and ``step`` for the composed
 MuonClip step."""
 from .api import *  # noqa: F401,F403
 from .api import __all__ as _api_all
-from .step import muonclip_step_mha, muonclip_step_mla  # noqa: F401
+from .step import CapturedStep, muonclip_step_mha, muonclip_step_mla  # noqa: F401
 
-__all__ = list(_api_all) + ["muonclip_step_mha", "muonclip_step_mla"]
+__all__ = list(_api_all) + ["CapturedStep", "muonclip_step_mha", "muonclip_step_mla"]

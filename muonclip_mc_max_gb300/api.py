@@ -95,7 +95,7 @@ def load_library():
         "mc_gemm_bf16": ([V, V, V, I, I, I, I, I, I, V], I),
         "mc_launch_count": ([], ctypes.c_ulonglong),
         "mc_trace_enable": ([I], I),
-        "mc_trace_collect": ([ctypes.POINTER(TraceEntry), I], I),
+        "mc_trace_collect": ([ctypes.POINTER(TraceEntry), I, I], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -374,13 +374,14 @@ def mc_trace_enable(on: bool = True):
     _check("mc_trace_enable", load_library().mc_trace_enable(int(on)))
 
 
-def mc_trace_collect() -> dict:
+def mc_trace_collect(keep: bool = False) -> dict:
     """{kernel kind: (launches, total_ms)} of the launches traced since the
-    last collect (event-timed on their launch streams)."""
+    last collect (event-timed on their launch streams).  keep=True leaves
+    the records in place (for replays of a captured graph)."""
     lib = load_library()
     cap = 64
     buf = (TraceEntry * cap)()
-    n = lib.mc_trace_collect(buf, cap)
+    n = lib.mc_trace_collect(buf, cap, int(keep))
     if n < 0:
         raise MCError("mc_trace_collect", 3, "CUDA error while reading trace events")
     return {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms))

@@ -130,11 +130,20 @@ static cudaEvent_t pooled_event() {
     return e;
 }
 
+// During stream capture an event becomes a graph node (re-recorded on every
+// replay) only when recorded as an external event.
+static void record_event(cudaEvent_t e, cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(s, &cs);
+    if (cs == cudaStreamCaptureStatusActive) cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+    else cudaEventRecord(e, s);
+}
+
 TraceScope::TraceScope(const char* name, cudaStream_t stream) : name_(name), stream_(stream), start_(nullptr) {
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (g_trace_on.load(std::memory_order_relaxed)) {
         start_ = pooled_event();
-        if (start_) cudaEventRecord(start_, stream_);
+        if (start_) record_event(start_, stream_);
     }
 }
 
@@ -142,7 +151,7 @@ TraceScope::~TraceScope() {
     if (!start_) return;
     cudaEvent_t end = pooled_event();
     if (!end) return;
-    cudaEventRecord(end, stream_);
+    record_event(end, stream_);
     std::lock_guard<std::mutex> lk(g_trace_mu);
     g_trace.push_back(TraceRec{name_, start_, end});
 }
@@ -226,11 +235,12 @@ mc_status mc_trace_enable(int on) {
     return MC_OK;
 }
 
-int mc_trace_collect(mc_trace_entry* out, int cap) {
+int mc_trace_collect(mc_trace_entry* out, int cap, int keep) {
     std::vector<TraceRec> recs;
     {
         std::lock_guard<std::mutex> lk(g_trace_mu);
-        recs.swap(g_trace);
+        if (keep) recs = g_trace;
+        else recs.swap(g_trace);
     }
     std::map<std::string, std::pair<long long, double>> agg;
     std::vector<std::string> order;
@@ -247,7 +257,7 @@ int mc_trace_collect(mc_trace_entry* out, int cap) {
             it->second.second += ms;
         }
     }
-    {
+    if (!keep) {
         std::lock_guard<std::mutex> lk(g_trace_mu);
         for (auto& r : recs) {
             g_event_pool.push_back(r.a);

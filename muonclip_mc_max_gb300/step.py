@@ -40,3 +40,33 @@ def muonclip_step_mla(x, w_qa, w_qb, w_kva, w_kb, H, nope, rope, rope_base, mast
                  eps=eps, nesterov=nesterov, workspace=workspace, stream=stream)
     gamma = mc_qk_clip_mla(masters[1], masters[3], H, nope, rope, s_max, tau, stream=stream)
     return s_max, gamma
+
+
+class CapturedStep:
+    """Captures a sequence of library calls (``fn``, launched on the current
+    stream) into one CUDA graph and replays it: the whole step costs one
+    graph launch on the host instead of one launch per kernel.
+
+    The calls are capture-safe: they only enqueue kernels and memsets on the
+    caller's stream and read device pointers that stay fixed, so inputs are
+    refreshed by copying into the same tensors before ``replay``.  ``fn`` is
+    run ``warmup`` times eagerly first (sizing workspaces outside capture)."""
+
+    def __init__(self, fn, warmup: int = 2):
+        import torch
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(warmup):
+                fn()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            fn()
+        torch.cuda.synchronize()
+
+    def replay(self):
+        self.graph.replay()
+
+    __call__ = replay
