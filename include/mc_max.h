@@ -104,6 +104,34 @@ mc_status mc_max_logits_mha(const void* x, const void* wq, const void* wk, mc_dt
                             float* s_max, float* s_max_bh, void* ws, size_t ws_bytes,
                             mc_stream_t stream);
 
+/*
+ * Allocation-free variant of mc_max_logits_mha.  The pages have no
+ * counterpart: this exists for callers that cannot allocate device memory
+ * at the point where they run the scan -- a plugin inside a host framework
+ * that owns every device allocation and forbids new ones while it enqueues
+ * work, or code that runs while its stream is being captured into a CUDA
+ * graph, where cudaMalloc is not allowed.  Such a caller cannot hand over a
+ * workspace, so this entry point uses scratch that lives in the library:
+ * one static device array of MC_NOALLOC_SCRATCH_BYTES, which every GPU that
+ * loads the library holds until the process exits.
+ *
+ * Same arguments, results and errors as mc_max_logits_mha, without ws and
+ * ws_bytes.  Sizes whose scratch (mc_max_logits_mha_workspace_size) exceeds
+ * MC_NOALLOC_SCRATCH_BYTES are rejected with MC_ERR_WORKSPACE before any
+ * work is enqueued.  The call allocates and frees nothing.
+ *
+ * The first call on a device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * Every call, on every stream, shares the one array and overwrites it (the
+ * parts that must start at zero are cleared by each call), so calls that
+ * overlap on the GPU race: serialise them, e.g. on one stream.
+ */
+#define MC_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+mc_status mc_max_logits_mha_noalloc(const void* x, const void* wq, const void* wk, mc_dtype dtype,
+                                    int B, int T, int D, int H, int dh, int causal,
+                                    int accumulate, float* s_max, float* s_max_bh,
+                                    mc_stream_t stream);
+
 /* An MLA attention layer's query/key projections (K2 / DeepSeek-V3 style;
  * the K2 review's MLA table names the components q^C, k^C, q^R, k^R):
  *   c_Q           = x W_qa                       W_qa  [D][q_lora]

@@ -19,7 +19,8 @@ from .build import library_path
 __all__ = [
     "MCError", "load_library", "header_symbols", "Workspace",
     "mc_status_string", "mc_read_device_status",
-    "mc_max_logits_mha", "mc_max_logits_mha_workspace_size",
+    "mc_max_logits_mha", "mc_max_logits_mha_workspace_size", "mc_max_logits_mha_noalloc",
+    "MC_NOALLOC_SCRATCH_BYTES",
     "mc_max_logits_mla", "mc_max_logits_mla_workspace_size",
     "mc_qk_clip_mha", "mc_qk_clip_mla", "mc_qk_clip_global",
     "mc_newton_schulz", "mc_newton_schulz_workspace_size",
@@ -30,6 +31,7 @@ __all__ = [
 
 MC_F32, MC_BF16 = 0, 1
 MC_DEV_NONFINITE, MC_DEV_TIMEOUT, MC_DEV_RANGE = 0x1, 0x2, 0x4
+MC_NOALLOC_SCRATCH_BYTES = 64 << 20  # static scratch of mc_max_logits_mha_noalloc
 # quintic Newton-Schulz coefficients ("Notes on Muon blog", "Algorithm")
 NS_COEFFS = (3.4445, -4.7750, 2.0315)
 
@@ -83,6 +85,7 @@ def load_library():
         "mc_read_device_status": ([V, ctypes.POINTER(U), I], I),
         "mc_max_logits_mha_workspace_size": ([I, I, I, I, I, I], S),
         "mc_max_logits_mha": ([V, V, V, I, I, I, I, I, I, I, I, V, V, V, S, V], I),
+        "mc_max_logits_mha_noalloc": ([V, V, V, I, I, I, I, I, I, I, I, V, V, V], I),
         "mc_max_logits_mla_workspace_size": ([ctypes.POINTER(MlaLayer), I, I], S),
         "mc_max_logits_mla": ([ctypes.POINTER(MlaLayer), V, I, I, I, I, V, V, V, S, V], I),
         "mc_qk_clip_mha": ([V, V, I, I, I, I, V, F, V, V], I),
@@ -196,6 +199,25 @@ def mc_max_logits_mha(x, wq, wk, H: int, dh: int, causal: bool = False, accumula
     _check("mc_max_logits_mha", lib.mc_max_logits_mha(
         _ptr(x), _ptr(wq), _ptr(wk), dt, B, T, D, H, dh, int(causal), int(accumulate),
         _ptr(s_max), _ptr(s_max_bh), ws, nb, _stream(stream)))
+    return s_max
+
+
+def mc_max_logits_mha_noalloc(x, wq, wk, H: int, dh: int, causal: bool = False,
+                              accumulate: bool = False, s_max=None, s_max_bh=None, stream=None):
+    """mc_max_logits_mha without a workspace: the library's static scratch
+    (MC_NOALLOC_SCRATCH_BYTES, shared by every call) is used instead, for
+    callers that may not allocate.  Pass s_max (and s_max_bh) preallocated
+    to allocate nothing here either."""
+    lib = load_library()
+    _need_cuda(x, wq, wk, s_max, s_max_bh)
+    B, T, D = x.shape
+    if wq.shape != (D, H * dh) or wk.shape != (D, H * dh):
+        raise ValueError("wq, wk must be [D, H*dh]")
+    if s_max is None:
+        s_max = torch.empty(H, dtype=torch.float32, device=x.device)
+    _check("mc_max_logits_mha_noalloc", lib.mc_max_logits_mha_noalloc(
+        _ptr(x), _ptr(wq), _ptr(wk), _dtype(x), B, T, D, H, dh, int(causal), int(accumulate),
+        _ptr(s_max), _ptr(s_max_bh), _stream(stream)))
     return s_max
 
 

@@ -356,6 +356,39 @@ mc_status mc_max_logits_mha(const void* x, const void* wq, const void* wk, mc_dt
     return MC_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free scan: the scratch is a static device array of the library
+// (one per device that loads it), so callers that may not allocate -- plugins
+// in frameworks that own all device memory, code running under stream
+// capture -- can still run the scan.  Its device address is looked up once
+// per device; all calls share the array, so overlapping calls race.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MC_NOALLOC_SCRATCH_BYTES];
+static void* g_noalloc_ptr[64];
+
+static void* noalloc_scratch() {
+    int dev = current_device();
+    if (dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        g_noalloc_ptr[dev] = p;
+    }
+    return g_noalloc_ptr[dev];
+}
+
+mc_status mc_max_logits_mha_noalloc(const void* x, const void* wq, const void* wk, mc_dtype dtype, int B, int T,
+                                    int D, int H, int dh, int causal, int accumulate, float* s_max,
+                                    float* s_max_bh, mc_stream_t stream) {
+    if (B <= 0 || T <= 0 || D <= 0 || H <= 0 || dh <= 0) return MC_ERR_INVALID_ARG;
+    if (mc_max_logits_mha_workspace_size(B, T, D, H, dh, dtype) > MC_NOALLOC_SCRATCH_BYTES) return MC_ERR_WORKSPACE;
+    void* scratch = noalloc_scratch();
+    if (!scratch) return MC_ERR_CUDA;
+    return mc_max_logits_mha(x, wq, wk, dtype, B, T, D, H, dh, causal, accumulate, s_max, s_max_bh, scratch,
+                             MC_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 static mc_status mla_check(const mc_mla_layer* L, bool scan) {
     if (!L) return MC_ERR_INVALID_ARG;
     if (L->D <= 0 || L->q_lora <= 0 || L->kv_lora <= 0 || L->H <= 0 || L->nope < 0 || L->rope < 0)
