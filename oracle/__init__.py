@@ -28,7 +28,8 @@ from .build import build as _build, library_path
 __all__ = [
     "NS_COEFFS", "load", "bf16_to_f64", "f64_to_bf16_bits", "max_logits_mha",
     "max_logits_mla", "gamma", "qk_clip_mha", "qk_clip_mla", "qk_clip_global",
-    "newton_schulz", "muon_step",
+    "newton_schulz", "muon_step", "max_logits_mha_np", "max_logits_mla_np", "newton_schulz_np",
+    "muon_step_np",
 ]
 
 # Quintic coefficients (a, b, c) of "Notes on Muon blog", section "Algorithm";
@@ -278,4 +279,103 @@ def muon_step(w, g, m, lr: float, mu: float = 0.95, wd: float = 0.1, rms: float 
                               a, b, c, eps, int(nesterov), _ptr(O))
     if rc:
         raise RuntimeError(f"oracle_muon_step failed ({rc})")
+    return W, M, O
+
+
+# ---------------------------------------------------------------------------
+# Library-GEMM restatements (numpy fp64 BLAS) for full-size sampled checks.
+# Same definitions, steps in the same order; the matrix products run in a
+# library routine so the large workloads finish in seconds.  Pinned against
+# the plain-loop C functions above (tests/test_oracle_pins.py).
+# ---------------------------------------------------------------------------
+
+def _rope_np(v: np.ndarray, pos0: int, base: float) -> np.ndarray:
+    """Rotate-half RoPE of rows v[t] at positions pos0 + t (fp64)."""
+    T, r = v.shape
+    h = r // 2
+    theta = base ** (-2.0 * np.arange(h) / r)
+    ang = (pos0 + np.arange(T))[:, None].astype(np.float64) * theta[None, :]
+    c, s = np.cos(ang), np.sin(ang)
+    lo, hi = v[:, :h], v[:, h:]
+    return np.concatenate([lo * c - hi * s, hi * c + lo * s], axis=1)
+
+
+def _pair_max(q: np.ndarray, k: np.ndarray, causal: bool, block: int = 1024) -> float:
+    """max over i, j (j <= i if causal) of q_i . k_j, computed in row blocks."""
+    T = q.shape[0]
+    best = -np.inf
+    for i0 in range(0, T, block):
+        i1 = min(T, i0 + block)
+        jend = i1 if causal else T
+        s = q[i0:i1] @ k[:jend].T
+        if causal:
+            s = np.where(np.arange(jend)[None, :] <= np.arange(i0, i1)[:, None], s, -np.inf)
+        if np.isnan(s).any():
+            return float("nan")
+        best = max(best, float(s.max()))
+    return best
+
+
+def max_logits_mha_np(x, wq, wk, H, dh, causal=False, heads=None, batches=None) -> np.ndarray:
+    """As max_logits_mha, with library GEMMs (fp64)."""
+    heads = list(range(H)) if heads is None else list(heads)
+    B = x.shape[0]
+    batches = list(range(B)) if batches is None else list(batches)
+    WQ, WK = _to_f64(wq), _to_f64(wk)
+    out = np.empty((len(batches), len(heads)))
+    for ib, b in enumerate(batches):
+        xb = _to_f64(x[b])
+        for ih, h in enumerate(heads):
+            q = xb @ WQ[:, h * dh:(h + 1) * dh]
+            k = xb @ WK[:, h * dh:(h + 1) * dh]
+            out[ib, ih] = _pair_max(q, k, causal) / np.sqrt(dh)
+    return out
+
+
+def max_logits_mla_np(x, w_qa, w_qb, w_kva, w_kb, H, nope, rope, rope_base, causal=True,
+                      heads=None, batches=None) -> np.ndarray:
+    """As max_logits_mla, with library GEMMs (fp64)."""
+    heads = list(range(H)) if heads is None else list(heads)
+    B = x.shape[0]
+    batches = list(range(B)) if batches is None else list(batches)
+    QA, QB, KVA, KB = _to_f64(w_qa), _to_f64(w_qb), _to_f64(w_kva), _to_f64(w_kb)
+    kvl = KVA.shape[1] - rope
+    qk = nope + rope
+    out = np.empty((len(batches), len(heads)))
+    for ib, b in enumerate(batches):
+        xb = _to_f64(x[b])
+        cq = xb @ QA
+        ckv = xb @ KVA
+        kr = _rope_np(ckv[:, kvl:], 0, rope_base)
+        for ih, h in enumerate(heads):
+            qh = cq @ QB[:, h * qk:(h + 1) * qk]
+            q = np.concatenate([qh[:, :nope], _rope_np(qh[:, nope:], 0, rope_base)], axis=1)
+            kc = ckv[:, :kvl] @ KB[:, h * nope:(h + 1) * nope]
+            k = np.concatenate([kc, kr], axis=1)
+            out[ib, ih] = _pair_max(q, k, causal) / np.sqrt(qk)
+    return out
+
+
+def newton_schulz_np(g, steps: int = 5, coeffs=NS_COEFFS, eps: float = 1e-7) -> np.ndarray:
+    """As newton_schulz, with library GEMMs (fp64)."""
+    G = _to_f64(g)
+    tr = G.shape[0] > G.shape[1]
+    X = G.T.copy() if tr else G.copy()
+    X /= np.sqrt(np.sum(X * X)) + eps
+    a, b, c = coeffs
+    for _ in range(steps):
+        A = X @ X.T
+        Bm = b * A + c * (A @ A)
+        X = a * X + Bm @ X
+    return X.T.copy() if tr else X
+
+
+def muon_step_np(w, g, m, lr: float, mu: float = 0.95, wd: float = 0.1, rms: float = 0.2,
+                 steps: int = 5, coeffs=NS_COEFFS, eps: float = 1e-7, nesterov: bool = False):
+    """As muon_step, with library GEMMs (fp64).  Returns (w_new, m_new, o)."""
+    W, G, M = _to_f64(w), _to_f64(g), _to_f64(m)
+    M = mu * M + G
+    U = G + mu * M if nesterov else M
+    O = newton_schulz_np(U, steps, coeffs, eps)
+    W = W - lr * (rms * np.sqrt(max(W.shape)) * O + wd * W)
     return W, M, O

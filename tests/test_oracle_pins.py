@@ -470,3 +470,38 @@ def test_muon_two_steps_equal_save_reload():
     saved_w, saved_m = wa.copy(), ma.copy()
     wc, mc, _ = oracle.muon_step(saved_w, g2, saved_m, lr=1e-2)
     assert np.array_equal(wb, wc) and np.array_equal(mb, mc)
+
+
+# ---------------------------------------------------------------------------
+# the library-GEMM restatements used for full-size sampled checks
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_np_mha_matches_c_oracle(causal):
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal((3, 70, 12))
+    wq, wk = rng.standard_normal((12, 4 * 5)), rng.standard_normal((12, 4 * 5))
+    a = oracle.max_logits_mha(x, wq, wk, 4, 5, causal, heads=[3, 0], batches=[2, 1])
+    b = oracle.max_logits_mha_np(x, wq, wk, 4, 5, causal, heads=[3, 0], batches=[2, 1])
+    np.testing.assert_allclose(b, a, rtol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_np_mla_matches_c_oracle(causal):
+    x, qa, qb, kva, kb = _mla_rand(32, 2, 1100, 10, 3, 6, 5, 4, 8)  # > one 1024-row block
+    a = oracle.max_logits_mla(x, qa, qb, kva, kb, 3, 4, 8, 50000.0, causal, heads=[2, 1])
+    b = oracle.max_logits_mla_np(x, qa, qb, kva, kb, 3, 4, 8, 50000.0, causal, heads=[2, 1])
+    np.testing.assert_allclose(b, a, rtol=1e-11)
+
+
+@pytest.mark.parametrize("shape", [(40, 24), (24, 40)])
+def test_np_muon_matches_c_oracle(shape):
+    rng = np.random.default_rng(33)
+    w, g, m = (rng.standard_normal(shape) for _ in range(3))
+    for nesterov in (False, True):
+        a = oracle.muon_step(w, g, m, lr=1e-3, nesterov=nesterov)
+        b = oracle.muon_step_np(w, g, m, lr=1e-3, nesterov=nesterov)
+        for u, v in zip(a, b):
+            np.testing.assert_allclose(v, u, rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(oracle.newton_schulz_np(g, 3), oracle.newton_schulz(g, 3),
+                               rtol=1e-10, atol=1e-13)
