@@ -49,6 +49,33 @@ MC_HD float key_float(uint32_t k) {
 #ifdef __CUDACC__
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: every library kernel is launched with
+// programmatic stream serialization, so its launch and prologue overlap the
+// tail of the previous kernel on the stream.  pdl_wait() blocks until that
+// kernel has completed and its writes are visible (it precedes every global
+// access); pdl_trigger() lets the next kernel start its prologue.
+// ---------------------------------------------------------------------------
+MC_D void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+MC_D void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // status word
 // ---------------------------------------------------------------------------
 MC_D void set_status(unsigned* status, unsigned bits) {

@@ -56,6 +56,7 @@ MC_D void scale8_f32(float* p, float f) {
 
 // grid (H, nseg, chunks): block (h, s) scales head h's columns of segment s
 __global__ void clip_kernel(const ClipArgs a) {
+    pdl_wait();
     const int h = blockIdx.x;
     const ClipSeg& sg = a.seg[blockIdx.y];
     const float g = clip_gamma(a.s_max[h], a.tau);
@@ -75,6 +76,7 @@ __global__ void clip_kernel(const ClipArgs a) {
             if (a.bf16) scale8_bf16(reinterpret_cast<__nv_bfloat16*>(sg.w) + off, f);
             else scale8_f32(reinterpret_cast<float*>(sg.w) + off, f);
         }
+        pdl_trigger();
     } else {
         const long long n = (long long)sg.rows * sg.width;
         for (long long i = (long long)blockIdx.z * blockDim.x + threadIdx.x; i < n;
@@ -89,6 +91,7 @@ __global__ void clip_kernel(const ClipArgs a) {
                 *p = __fmul_rn(*p, f);
             }
         }
+        pdl_trigger();
     }
 }
 
@@ -105,14 +108,14 @@ cudaError_t launch_clip(const ClipArgs& a, cudaStream_t stream) {
     if (chunks > 64) chunks = 64;
     dim3 grid(a.H, a.nseg, (unsigned)chunks);
     TraceScope ts("clip", stream);
-    clip_kernel<<<grid, threads, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(clip_kernel, grid, dim3(threads), 0, stream, a);
 }
 
 // Global clip: gamma from max_h s_max[h] (NaN propagates), then every
 // element of wq x gamma^alpha and of wk x gamma^(1-alpha).
 __global__ void clip_global_kernel(void* wq, void* wk, int bf16, long long n, const float* s_max, int H,
                                    float tau, float alpha, float* gamma_out) {
+    pdl_wait();
     float s = s_max[0];
     for (int h = 1; h < H; ++h) s = max_nan(s, s_max[h]);
     const float g = clip_gamma(s, tau);
@@ -134,6 +137,7 @@ __global__ void clip_global_kernel(void* wq, void* wk, int bf16, long long n, co
             *k = __fmul_rn(*k, fk);
         }
     }
+    pdl_trigger();
 }
 
 cudaError_t launch_clip_global(void* wq, void* wk, int bf16, long long n, const float* s_max, int H, float tau,
@@ -143,15 +147,15 @@ cudaError_t launch_clip_global(void* wq, void* wk, int bf16, long long n, const 
     if (blocks > 4096) blocks = 4096;
     if (blocks < 1) blocks = 1;
     TraceScope ts("clip_global", stream);
-    clip_global_kernel<<<(unsigned)blocks, threads, 0, stream>>>(wq, wk, bf16, n, s_max, H, tau, alpha,
-                                                                 gamma_out);
-    return cudaGetLastError();
+    return launch_pdl(clip_global_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream, wq, wk, bf16, n,
+                      s_max, H, tau, alpha, gamma_out);
 }
 
 // ---------------------------------------------------------------------------
 // bf16 -> fp16 (weights feeding an fp16 contraction)
 // ---------------------------------------------------------------------------
 __global__ void bf16_to_f16_kernel(const __nv_bfloat16* __restrict__ src, __half* __restrict__ dst, long long n) {
+    pdl_wait();
     const long long nv = n / 8;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += (long long)gridDim.x * blockDim.x) {
         uint4 u = reinterpret_cast<const uint4*>(src)[i];
@@ -165,6 +169,7 @@ __global__ void bf16_to_f16_kernel(const __nv_bfloat16* __restrict__ src, __half
     for (long long i = nv * 8 + (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (long long)gridDim.x * blockDim.x)
         dst[i] = __float2half_rn(__bfloat162float(src[i]));
+    pdl_trigger();
 }
 
 cudaError_t launch_bf16_to_f16(const void* src, void* dst, long long n, cudaStream_t stream) {
@@ -174,8 +179,8 @@ cudaError_t launch_bf16_to_f16(const void* src, void* dst, long long n, cudaStre
     if (blocks < 1) blocks = 1;
     if (blocks > (long long)num_sms() * 8) blocks = (long long)num_sms() * 8;
     TraceScope ts("to_f16", stream);
-    bf16_to_f16_kernel<<<(unsigned)blocks, threads, 0, stream>>>((const __nv_bfloat16*)src, (__half*)dst, n);
-    return cudaGetLastError();
+    return launch_pdl(bf16_to_f16_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream,
+                      (const __nv_bfloat16*)src, (__half*)dst, n);
 }
 
 // ---------------------------------------------------------------------------
@@ -195,6 +200,7 @@ __global__ void __launch_bounds__(kMatThreads) mat_pass_kernel(const __grid_cons
     __shared__ float U[kTile][kTile + 1];
     __shared__ double red[kMatThreads / 32];
     const int tid = threadIdx.x;
+    pdl_wait();
     for (int t = blockIdx.x; t < B.total_tiles; t += gridDim.x) {
         int di;
         find_mat(B, t, di);
@@ -310,6 +316,7 @@ __global__ void __launch_bounds__(kMatThreads) mat_pass_kernel(const __grid_cons
             __syncthreads();
         }
     }
+    pdl_trigger();
 }
 
 cudaError_t launch_mat_pass(const MatBatch& b, cudaStream_t stream) {
@@ -318,12 +325,12 @@ cudaError_t launch_mat_pass(const MatBatch& b, cudaStream_t stream) {
     if (grid > b.total_tiles) grid = b.total_tiles;
     static const char* names[4] = {"muon_momentum", "ns_cast", "muon_update", "ns_out"};
     TraceScope ts(names[b.mode & 3], stream);
-    mat_pass_kernel<<<grid, kMatThreads, 0, stream>>>(b);
-    return cudaGetLastError();
+    return launch_pdl(mat_pass_kernel, dim3(grid), dim3(kMatThreads), 0, stream, b);
 }
 
 // s = 1 / (||U||_F + eps) from the tile partials, summed in a fixed order
 __global__ void norm_finalize_kernel(const __grid_constant__ NormArgs a) {
+    pdl_wait();
     const int z = blockIdx.x;
     if (z >= a.count) return;
     __shared__ double red[256];
@@ -340,13 +347,13 @@ __global__ void norm_finalize_kernel(const __grid_constant__ NormArgs a) {
         a.s[z] = (float)(1.0 / den);
         a.s2[z] = (float)(1.0 / (den * den));
     }
+    pdl_trigger();
 }
 
 cudaError_t launch_norm_finalize(const NormArgs& a, cudaStream_t stream) {
     if (a.count <= 0) return cudaSuccess;
     TraceScope ts("norm_finalize", stream);
-    norm_finalize_kernel<<<a.count, 256, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(norm_finalize_kernel, dim3(a.count), dim3(256), 0, stream, a);
 }
 
 }  // namespace mc

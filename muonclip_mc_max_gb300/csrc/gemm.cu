@@ -19,7 +19,13 @@ namespace mc {
 constexpr int kAStageBytes = kBM * kBK * 2;  // 16 KB
 constexpr int kBStageBytes = kBN * kBK * 2;  // 32 KB
 constexpr int kGemmThreads = 192;
-constexpr int kGemmSmem = kGemmStages * (kAStageBytes + kBStageBytes) + 1024 + 256;
+// epilogue staging: each epilogue warp stages a 32 x 64 chunk of 16-bit
+// values in rows of 72 elements (144 B: 16-byte accesses are bank-conflict
+// free) so that every global load/store of the epilogue is a coalesced
+// 16-byte access by 8 lanes per 128-byte row segment
+constexpr int kStageLd = 72;
+constexpr int kEpiWarpBytes = 32 * kStageLd * 2;  // 4608 B
+constexpr int kGemmSmem = kGemmStages * (kAStageBytes + kBStageBytes) + 4 * kEpiWarpBytes + 1024 + 256;
 
 struct GemmSmemTail {
     uint64_t full[kGemmStages];
@@ -165,12 +171,133 @@ MC_D void epilogue_chunk(const GemmProblem& q, int z, int r, int col0, float* f,
     }
 }
 
+MC_D uint4 pack8(const float* v, bool f16) {
+    uint4 u;
+    if (f16) {
+        __half2* h = reinterpret_cast<__half2*>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+    } else {
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    }
+    return u;
+}
+
+// Warp-cooperative epilogue of a 32-row x 64-column chunk (rows row0.., one
+// per lane; 16-bit output with vec_ok).  Aux rows are fetched with coalesced
+// 16-byte loads into the warp's staging buffer S, the results are staged
+// back into S, then written with coalesced 16-byte stores: the rows, and for
+// symmetric outputs the mirrored rows (c, r) of every c >= r.  Only the
+// 16-byte segment that straddles the diagonal is written element-wise.
+MC_D void epilogue_chunk_staged(const GemmProblem& q, int z, int row0, int col0, float* f, float sc,
+                                uint16_t* S, unsigned* status) {
+    const int lane = threadIdx.x & 31;
+    const int r = row0 + lane;
+    if (col0 >= q.N) return;  // warp-uniform
+    __syncwarp();             // every lane is done with the previous chunk's S
+    const int seg = lane & 7, sub = lane >> 3;
+    if (q.rope_tab && (col0 % q.rope_period) == q.rope_start && r < q.M) {
+        const float2* cs = q.rope_tab + (size_t)(r % q.rope_T) * 32;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            float2 t = cs[i];
+            float lo = f[i], hi = f[i + 32];
+            f[i] = lo * t.x - hi * t.y;
+            f[i + 32] = hi * t.x + lo * t.y;
+        }
+    }
+    if (q.aux) {
+        const __nv_bfloat16* ab = q.aux + (size_t)z * q.aux_bstride + col0 + seg * 8;
+        uint4 u[8];
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+            const int rr = it * 4 + sub, grow = row0 + rr;
+            u[it] = (grow < q.M && col0 + seg * 8 < q.N)
+                        ? *reinterpret_cast<const uint4*>(ab + (size_t)grow * q.aux_ld)
+                        : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int it = 0; it < 8; ++it) *reinterpret_cast<uint4*>(S + (it * 4 + sub) * kStageLd + seg * 8) = u[it];
+        __syncwarp();
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+            uint4 w = *reinterpret_cast<const uint4*>(S + lane * kStageLd + v * 8);
+            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float2 a2 = __bfloat1622float2(h[i]);
+                f[8 * v + 2 * i] = sc * (q.alpha * f[8 * v + 2 * i] + q.beta * a2.x);
+                f[8 * v + 2 * i + 1] = sc * (q.alpha * f[8 * v + 2 * i + 1] + q.beta * a2.y);
+            }
+        }
+        __syncwarp();
+    } else if (q.alpha != 1.0f || sc != 1.0f) {
+        const float s2 = sc * q.alpha;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) f[i] *= s2;
+    }
+    const bool f16 = q.out_kind == kOutF16;
+    if (f16) {
+        bool big = false;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) big |= fabsf(f[i]) > 65504.0f;
+        if (big) set_status(status, MC_DEV_RANGE);
+    }
+#pragma unroll
+    for (int v = 0; v < 8; ++v) *reinterpret_cast<uint4*>(S + lane * kStageLd + v * 8) = pack8(f + 8 * v, f16);
+    __syncwarp();
+    uint16_t* ob = reinterpret_cast<uint16_t*>(q.out) + (size_t)z * q.out_bstride;
+    // rows: 8 passes of 4 rows x 8 segments
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int rr = it * 4 + sub, grow = row0 + rr, c = col0 + seg * 8;
+        if (grow >= q.M || c >= q.N) continue;
+        const uint4 u = *reinterpret_cast<const uint4*>(S + rr * kStageLd + seg * 8);
+        uint16_t* dst = ob + (size_t)grow * q.out_ld + c;
+        if (!q.sym || c >= grow) {
+            *reinterpret_cast<uint4*>(dst) = u;
+        } else if (c + 7 >= grow) {
+            const uint16_t* e = reinterpret_cast<const uint16_t*>(&u);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (c + i >= grow) dst[i] = e[i];
+        }
+    }
+    if (!q.sym) return;
+    // mirror: output row c (col0 <= c < col0 + 64) gets columns row0..row0+31,
+    // 8 per lane (4 lanes per row, 8 rows per pass)
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int cc = it * 8 + (lane >> 2), rs = (lane & 3) * 8;
+        const int c = col0 + cc, r0 = row0 + rs;
+        if (c >= q.N || r0 >= q.M || c < r0) continue;  // all 8 have c < r: the row pass wrote them
+        uint16_t e[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) e[i] = S[(rs + i) * kStageLd + cc];
+        uint16_t* dst = ob + (size_t)c * q.out_ld + r0;
+        if (c >= r0 + 7) {
+            uint4 u;
+            uint16_t* pu = reinterpret_cast<uint16_t*>(&u);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) pu[i] = e[i];
+            *reinterpret_cast<uint4*>(dst) = u;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (r0 + i <= c) dst[i] = e[i];
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParams P) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + kGemmStages * kAStageBytes;
-    GemmSmemTail* tail = reinterpret_cast<GemmSmemTail*>(sB + kGemmStages * kBStageBytes);
+    uint16_t* sEpi = reinterpret_cast<uint16_t*>(sB + kGemmStages * kBStageBytes);
+    GemmSmemTail* tail = reinterpret_cast<GemmSmemTail*>(sB + kGemmStages * kBStageBytes + 4 * kEpiWarpBytes);
     volatile int* abort_flag = &tail->abort_flag;
 
     const int warp = threadIdx.x >> 5;
@@ -203,6 +330,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = tail->tmem_base;
+    pdl_wait();  // the previous kernel's outputs are our inputs
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
@@ -309,8 +437,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             const GemmProblem& q = P.p[pi];
             if (!mbar_wait(&tail->tfull[acc], aphase, abort_flag, P.status)) break;
             tc_fence_after();
-            const int r = tm * kBM + quarter * 32 + lane;
+            const int row0 = tm * kBM + quarter * 32;
+            const int r = row0 + lane;
             const float sc = q.scale ? q.scale[z] : 1.0f;
+            const bool staged = q.vec_ok && q.out_kind != kOutF32;
+            uint16_t* S = sEpi + (warp - 2) * (32 * kStageLd);
 #pragma unroll 1
             for (int c = 0; c < kBN / 64; ++c) {
                 uint32_t v[64];
@@ -318,7 +449,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 tmem_ld32(taddr, v);
                 tmem_ld32(taddr + 32, v + 32);
                 tmem_ld_wait();
-                epilogue_chunk(q, z, r, tn * kBN + c * 64, reinterpret_cast<float*>(v), sc, P.status);
+                if (staged)
+                    epilogue_chunk_staged(q, z, row0, tn * kBN + c * 64, reinterpret_cast<float*>(v), sc, S,
+                                          P.status);
+                else
+                    epilogue_chunk(q, z, r, tn * kBN + c * 64, reinterpret_cast<float*>(v), sc, P.status);
             }
             tc_fence_before();
             __syncwarp();
@@ -330,6 +465,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         }
     }
 
+    pdl_trigger();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -349,8 +485,7 @@ cudaError_t launch_gemm(const GemmParams& P, cudaStream_t stream, const char* la
     int grid = num_sms();
     if (grid > P.total_tiles) grid = P.total_tiles;
     TraceScope ts(label, stream);
-    gemm_kernel<<<grid, kGemmThreads, kGemmSmem, stream>>>(P);
-    return cudaGetLastError();
+    return launch_pdl(gemm_kernel, dim3(grid), dim3(kGemmThreads), kGemmSmem, stream, P);
 }
 
 }  // namespace mc

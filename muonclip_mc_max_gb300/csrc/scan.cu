@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = tail->tmem_base;
+    pdl_wait();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -273,6 +274,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(const __grid_cons
         }
     }
 
+    pdl_trigger();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -319,8 +321,7 @@ cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream) {
     int grid = num_sms();
     if (grid > P.total_items) grid = P.total_items;
     TraceScope ts("scan", stream);
-    scan_kernel<<<grid, kScanThreads, kScanSmem, stream>>>(P);
-    return cudaGetLastError();
+    return launch_pdl(scan_kernel, dim3(grid), dim3(kScanThreads), kScanSmem, stream, P);
 }
 
 // ---------------------------------------------------------------------------
@@ -336,12 +337,14 @@ MC_D float load_f<__nv_bfloat16>(const __nv_bfloat16* p, size_t i) { return __bf
 template <typename T>
 __global__ void proj_simt_kernel(const T* __restrict__ x, const T* __restrict__ w, float* __restrict__ out,
                                  int rows, int D, int N) {
+    pdl_wait();
     size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (size_t)rows * N) return;
     int r = (int)(idx / N), c = (int)(idx % N);
     float s = 0.f;
     for (int k = 0; k < D; ++k) s = fmaf(load_f(x, (size_t)r * D + k), load_f(w, (size_t)k * N + c), s);
     out[idx] = s;
+    pdl_trigger();
 }
 
 cudaError_t launch_proj_simt(const void* x, const void* w, mc_dtype dt, float* out, int rows, int D,
@@ -351,16 +354,16 @@ cudaError_t launch_proj_simt(const void* x, const void* w, mc_dtype dt, float* o
     unsigned blocks = (unsigned)((n + threads - 1) / threads);
     TraceScope ts("proj_simt", stream);
     if (dt == MC_F32)
-        proj_simt_kernel<float><<<blocks, threads, 0, stream>>>((const float*)x, (const float*)w, out, rows, D, N);
-    else
-        proj_simt_kernel<__nv_bfloat16><<<blocks, threads, 0, stream>>>(
-            (const __nv_bfloat16*)x, (const __nv_bfloat16*)w, out, rows, D, N);
-    return cudaGetLastError();
+        return launch_pdl(proj_simt_kernel<float>, dim3(blocks), dim3(threads), 0, stream, (const float*)x,
+                          (const float*)w, out, rows, D, N);
+    return launch_pdl(proj_simt_kernel<__nv_bfloat16>, dim3(blocks), dim3(threads), 0, stream,
+                      (const __nv_bfloat16*)x, (const __nv_bfloat16*)w, out, rows, D, N);
 }
 
 // one thread per (b, h, i): max over j of q_i . k_j (fp32), q/k [B*T][H*dh]
 __global__ void scan_simt_kernel(const float* __restrict__ q, const float* __restrict__ k, int B, int T,
                                  int H, int dh, int causal, unsigned* __restrict__ keys) {
+    pdl_wait();
     size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (size_t)B * H * T) return;
     int i = (int)(idx % T);
@@ -377,6 +380,7 @@ __global__ void scan_simt_kernel(const float* __restrict__ q, const float* __res
         m = max_nan(m, s);
     }
     atomicMax(&keys[b * H + h], float_key(m));
+    pdl_trigger();
 }
 
 cudaError_t launch_scan_simt(const float* q, const float* k, int B, int T, int H, int dh, int causal,
@@ -385,8 +389,7 @@ cudaError_t launch_scan_simt(const float* q, const float* k, int B, int T, int H
     int threads = 128;
     unsigned blocks = (unsigned)((n + threads - 1) / threads);
     TraceScope ts("scan_simt", stream);
-    scan_simt_kernel<<<blocks, threads, 0, stream>>>(q, k, B, T, H, dh, causal, keys);
-    return cudaGetLastError();
+    return launch_pdl(scan_simt_kernel, dim3(blocks), dim3(threads), 0, stream, q, k, B, T, H, dh, causal, keys);
 }
 
 // ---------------------------------------------------------------------------
@@ -395,6 +398,7 @@ cudaError_t launch_scan_simt(const float* q, const float* k, int B, int T, int H
 __global__ void finalize_smax_kernel(const unsigned* __restrict__ keys, int B, int H, float sqrt_d,
                                      int accumulate, float* __restrict__ s_max, float* __restrict__ s_bh,
                                      unsigned* status) {
+    pdl_wait();
     int h = blockIdx.x * blockDim.x + threadIdx.x;
     if (h >= H) return;
     unsigned best = 0;
@@ -407,6 +411,7 @@ __global__ void finalize_smax_kernel(const unsigned* __restrict__ keys, int B, i
     if (accumulate) s = max_nan(s_max[h], s);
     if (!isfinite(s)) set_status(status, MC_DEV_NONFINITE);
     s_max[h] = s;
+    pdl_trigger();
 }
 
 cudaError_t launch_finalize_smax(const unsigned* keys, int B, int H, float d, int accumulate, float* s_max,
@@ -414,29 +419,36 @@ cudaError_t launch_finalize_smax(const unsigned* keys, int B, int H, float d, in
     int threads = 64;
     int blocks = (H + threads - 1) / threads;
     TraceScope ts("finalize_smax", stream);
-    finalize_smax_kernel<<<blocks, threads, 0, stream>>>(keys, B, H, sqrtf(d), accumulate, s_max, s_bh,
-                                                         device_status_ptr());
-    return cudaGetLastError();
+    return launch_pdl(finalize_smax_kernel, dim3(blocks), dim3(threads), 0, stream, keys, B, H, sqrtf(d),
+                      accumulate, s_max, s_bh, device_status_ptr());
 }
 
-// (cos, sin)(t * base^(-2f/64)), formed in double so that positions up to
-// the longest sequences keep full float accuracy
+// (cos, sin)(t * base^(-2f/64)).  The angle is formed in double in units of
+// pi and reduced exactly to [-1, 1] (subtracting an even integer is exact),
+// so positions up to the longest sequences keep float accuracy; one float
+// sincospi per entry then does the rest.
 __global__ void rope_table_kernel(float2* tab, int T, double base) {
+    __shared__ double th[32];  // theta_f / pi
+    if (threadIdx.x < 32) th[threadIdx.x] = pow(base, -2.0 * (double)threadIdx.x / 64.0) / M_PI;
+    __syncthreads();
+    pdl_wait();
     int idx = blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= T * 32) return;
-    int t = idx >> 5, f = idx & 31;
-    double theta = pow(base, -2.0 * (double)f / 64.0);
-    double s, c;
-    sincos((double)t * theta, &s, &c);
-    tab[idx] = make_float2((float)c, (float)s);
+    if (idx < T * 32) {
+        int t = idx >> 5, f = idx & 31;
+        double x = (double)t * th[f];
+        x -= 2.0 * rint(0.5 * x);
+        float sn, cs;
+        sincospif((float)x, &sn, &cs);
+        tab[idx] = make_float2(cs, sn);
+    }
+    pdl_trigger();
 }
 
 cudaError_t launch_rope_table(float2* tab, int T, float base, cudaStream_t stream) {
     int threads = 256;
     int blocks = (T * 32 + threads - 1) / threads;
     TraceScope ts("rope_table", stream);
-    rope_table_kernel<<<blocks, threads, 0, stream>>>(tab, T, (double)base);
-    return cudaGetLastError();
+    return launch_pdl(rope_table_kernel, dim3(blocks), dim3(threads), 0, stream, tab, T, (double)base);
 }
 
 }  // namespace mc
