@@ -56,6 +56,24 @@ def scan_pairs(B, T, causal):
     return B * (T * (T + 1) // 2 if causal else T * T)
 
 
+# DRAM bytes (read + write) per launch of each kernel kind, from the ncu
+# captures summarised in profiles/ (cold-cache replays).  Workloads captured
+# on a smaller case are scaled by the units processed (matrices, sequences),
+# which their traffic grows in proportion to.  Drop an entry whenever the
+# kernel changes after the capture.
+TRAFFIC = {
+    ("c2", "gemm:ns_gram"): 4269824,
+    ("c2", "gemm:ns_poly"): 4270080,
+    ("c2", "gemm:ns_apply"): 8464384,
+    ("c2", "scan"): 33599488,
+    ("c4", "gemm:ns_gram"): int((297524224 + 44363008) * 12),
+    ("c4", "gemm:ns_poly"): int((67321856 + 23865344) * 12),
+    ("c4", "gemm:ns_apply"): int((353615360 + 208807424) * 12),
+    ("c4", "muon_momentum"): 3758299648 + 2768514048,
+    ("c3", "scan"): int((231511296 + 3700224) * 16),
+}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -495,12 +513,14 @@ def run_ours(args, wl):
     if kind == "tensor":
         achieved = work / n_launch / dur / 1e12
         roof = {"kernel": dominant, "bound": "tensor", "achieved": achieved, "peak": bf16_peak,
-                "unit": "TFLOP/s", "frac": achieved / bf16_peak, "traffic": None,
+                "unit": "TFLOP/s", "frac": achieved / bf16_peak,
+                "traffic": TRAFFIC.get((wl.name, dominant)),
                 "peak_kind": f"{peak_src} bf16 dense (burst)"}
     else:
         achieved = work / n_launch / dur / 1e9
         roof = {"kernel": dominant, "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
-                "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": None,
+                "unit": "GB/s", "frac": achieved / hbm_peak,
+                "traffic": TRAFFIC.get((wl.name, dominant)),
                 "peak_kind": f"{peak_src} HBM copy"}
     assert api.mc_read_device_status(clear=True) == 0, "device status set during timing"
 
@@ -579,9 +599,15 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c2")
     ap.add_argument("--experts", type=int, default=48,
                     help="c4: up- and down-projections each (smaller for profiling)")
+    ap.add_argument("--seqs", type=int, default=None, help="c3/c5: sequences (smaller for profiling)")
+    ap.add_argument("--tokens", type=int, default=None, help="c3/c5: tokens per sequence")
     args = ap.parse_args()
-    wl = (ExpertBatch(args.experts, args.experts) if args.workload == "c4"
-          else WORKLOADS[args.workload]())
+    if args.workload == "c4":
+        wl = ExpertBatch(args.experts, args.experts)
+    elif args.workload in ("c3", "c5"):
+        wl = MlaLayer(args.workload, B=args.seqs, T=args.tokens)
+    else:
+        wl = WORKLOADS[args.workload]()
     if args.impl == "reference":
         run_reference(args, wl)
     else:
