@@ -62,13 +62,7 @@ def scan_pairs(B, T, causal):
 # which their traffic grows in proportion to.  Drop an entry whenever the
 # kernel changes after the capture.
 TRAFFIC = {
-    ("c2", "gemm:ns_gram"): 4269824,
-    ("c2", "gemm:ns_poly"): 4270080,
-    ("c2", "gemm:ns_apply"): 8464384,
     ("c2", "scan"): 33599488,
-    ("c4", "gemm:ns_gram"): int((297524224 + 44363008) * 12),
-    ("c4", "gemm:ns_poly"): int((67321856 + 23865344) * 12),
-    ("c4", "gemm:ns_apply"): int((353615360 + 208807424) * 12),
     ("c4", "muon_momentum"): 3758299648 + 2768514048,
     ("c3", "scan"): int((231511296 + 3700224) * 16),
 }
@@ -117,15 +111,13 @@ class MhaLayer(Workload):
         self.units = {
             "gemm:proj": ("tensor", 2 * 2 * B * T * D * N),
             "scan": ("tensor", 2 * scan_pairs(B, T, False) * H * dh),
-            "gemm:ns_gram": ("tensor", 5 * 2 * ns["gram"]),
-            "gemm:ns_poly": ("tensor", 5 * 2 * ns["poly"]),
-            "gemm:ns_apply": ("tensor", 5 * 2 * ns["apply"]),
+            # all 5 quintic iterations (15 GEMM phases) run as one launch
+            "gemm:ns": ("tensor", 5 * 2 * (ns["gram"] + ns["poly"] + ns["apply"])),
             "muon_momentum": ("hbm", 2 * D * N * 14),
             "muon_update": ("hbm", 2 * D * N * 10),
         }
         self.scan_flops = self.units["gemm:proj"][1] + self.units["scan"][1]
-        self.ns_flops = sum(self.units[k][1] for k in ("gemm:ns_gram", "gemm:ns_poly",
-                                                      "gemm:ns_apply"))
+        self.ns_flops = self.units["gemm:ns"][1]
 
     def make(self, device):
         inp = mc_inputs.c2(device=device, B=self.B, T=self.T, D=self.D, H=self.H, dh=self.dh)
@@ -189,15 +181,12 @@ class ExpertBatch(Workload):
         ns = ns_flops_per_iter(2048, 7168)
         cnt = n_up + n_down
         self.units = {
-            "gemm:ns_gram": ("tensor", 5 * ns["gram"] * cnt),
-            "gemm:ns_poly": ("tensor", 5 * ns["poly"] * cnt),
-            "gemm:ns_apply": ("tensor", 5 * ns["apply"] * cnt),
+            "gemm:ns": ("tensor", 5 * (ns["gram"] + ns["poly"] + ns["apply"]) * cnt),
             "muon_momentum": ("hbm", cnt * 2048 * 7168 * 14),
             "muon_update": ("hbm", cnt * 2048 * 7168 * 10),
         }
         self.scan_flops = 0
-        self.ns_flops = (self.units["gemm:ns_gram"][1] + self.units["gemm:ns_poly"][1]
-                         + self.units["gemm:ns_apply"][1])
+        self.ns_flops = self.units["gemm:ns"][1]
 
     def make(self, device):
         return mc_inputs.c4(device=device, n_up=self.n_up, n_down=self.n_down)

@@ -19,6 +19,7 @@ namespace mc {
 __device__ unsigned g_status_word;  // per-device status bits (MC_DEV_*)
 
 static std::mutex g_mu;
+static std::mutex g_launch_mu;  // guards the static multi-phase parameter block
 static unsigned* g_status_ptr[64];
 static int g_sms[64];
 
@@ -85,15 +86,18 @@ bool make_tmap_3d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t ou
     return r == CUDA_SUCCESS;
 }
 
-void finalize_gemm_params(GemmParams& P) {
+template <int MAXP>
+void finalize_gemm_params(GemmParamsT<MAXP>& P) {
     int begin = 0;
+    if (P.bn <= 0) P.bn = kBN;
     for (int i = 0; i < P.nprob; ++i) {
         GemmProblem& q = P.p[i];
         q.tiles_m = (q.M + kBM - 1) / kBM;
-        q.tiles_n = (q.N + kBN - 1) / kBN;
+        q.tiles_n = (q.N + P.bn - 1) / P.bn;
         if (q.sym) {
+            // row block tm keeps the column tiles that reach the diagonal
             int t = 0;
-            for (int tm = 0; tm < q.tiles_m; ++tm) t += q.tiles_n - tm / 2;
+            for (int tm = 0; tm < q.tiles_m; ++tm) t += q.tiles_n - (kBM * tm) / P.bn;
             q.tiles_per_batch = t;
         } else {
             q.tiles_per_batch = q.tiles_m * q.tiles_n;
@@ -103,7 +107,14 @@ void finalize_gemm_params(GemmParams& P) {
     }
     P.total_tiles = begin;
     P.status = device_status_ptr();
+    if (P.nphase <= 0) {
+        P.nphase = 1;
+        P.phase_prob[0] = 0;
+        P.phase_prob[1] = P.nprob;
+    }
 }
+template void finalize_gemm_params<kMaxProblems>(GemmParamsT<kMaxProblems>&);
+template void finalize_gemm_params<kMaxProblemsMulti>(GemmParamsT<kMaxProblemsMulti>&);
 
 // ---------------------------------------------------------------------------
 // launch counting and optional event tracing
@@ -590,6 +601,7 @@ struct NsPlan {
     std::vector<int> nparts;
     float* s;
     float* s2;
+    unsigned* bar;  // grid-barrier counter of the multi-phase launches
     size_t bytes;
 };
 
@@ -635,6 +647,7 @@ bool plan_ns(const int* rows, const int* cols, int count, uint8_t* base, NsPlan&
         }
     P.s = c.take<float>(count);
     P.s2 = c.take<float>(count);
+    P.bar = c.take<unsigned>(1);
     P.bytes = c.used;
     return true;
 }
@@ -719,63 +732,93 @@ mc_status run_norm(const NsPlan& P, float eps, cudaStream_t stream) {
     return MC_OK;
 }
 
+// One Newton-Schulz GEMM of iteration `it` for a shape group:
 // kind 0: Gram A = sc2 X X^T ; 1: poly B = c A A + b A ; 2: apply X' = sc (B X + a X)
-mc_status run_ns_phase(const NsPlan& P, int kind, int it, float a, float b, float c, cudaStream_t stream) {
+bool ns_problem(GemmProblem& q, const NsPlan& P, const NsGroup& gr, int kind, int it, float a, float b,
+                float c, int bn) {
+    memset(&q, 0, sizeof(q));
     const int xin = it & 1, xout = (it + 1) & 1;
-    for (size_t g0 = 0; g0 < P.groups.size(); g0 += kMaxProblems) {
-        GemmParams G;
-        memset(&G, 0, sizeof(G));
-        for (size_t gi = g0; gi < std::min(P.groups.size(), g0 + kMaxProblems); ++gi) {
-            const NsGroup& gr = P.groups[gi];
-            GemmProblem& q = G.p[G.nprob++];
-            const uint64_t cnt = gr.idx.size(), mp = gr.m_pad, np = gr.n_pad;
-            q.batch = (int)cnt;
-            q.vec_ok = 1;
-            if (kind == 0) {
-                if (!make_tmap_3d(&q.tmA, gr.X[xin], np, mp, cnt, np, mp * np, kBK, kBM, 0)) return MC_ERR_CUDA;
-                if (!make_tmap_3d(&q.tmB, gr.X[xin], np, mp, cnt, np, mp * np, kBK, kBN, 0)) return MC_ERR_CUDA;
-                q.M = q.N = (int)mp;
-                q.K = (int)np;
-                q.sym = 1;
-                q.out = gr.A;
-                q.out_ld = mp;
-                q.out_bstride = mp * mp;
-                q.alpha = 1.f;
-                q.scale = it == 0 ? P.s2 + gr.zbase : nullptr;
-            } else if (kind == 1) {
-                if (!make_tmap_3d(&q.tmA, gr.A, mp, mp, cnt, mp, mp * mp, kBK, kBM, 0)) return MC_ERR_CUDA;
-                if (!make_tmap_3d(&q.tmB, gr.A, mp, mp, cnt, mp, mp * mp, kBK, kBN, 0)) return MC_ERR_CUDA;
-                q.M = q.N = q.K = (int)mp;
-                q.sym = 1;
-                q.out = gr.Bm;
-                q.out_ld = mp;
-                q.out_bstride = mp * mp;
-                q.aux = gr.A;
-                q.aux_ld = mp;
-                q.aux_bstride = mp * mp;
-                q.alpha = c;
-                q.beta = b;
-            } else {
-                if (!make_tmap_3d(&q.tmA, gr.Bm, mp, mp, cnt, mp, mp * mp, kBK, kBM, 0)) return MC_ERR_CUDA;
-                if (!make_tmap_3d(&q.tmB, gr.X[xin], np, mp, cnt, np, mp * np, 64, kBK, 0)) return MC_ERR_CUDA;
-                q.b_mn = 1;
-                q.M = (int)mp;
-                q.N = (int)np;
-                q.K = (int)mp;
-                q.out = gr.X[xout];
-                q.out_ld = np;
-                q.out_bstride = mp * np;
-                q.aux = gr.X[xin];
-                q.aux_ld = np;
-                q.aux_bstride = mp * np;
-                q.alpha = 1.f;
-                q.beta = a;
-                q.scale = it == 0 ? P.s + gr.zbase : nullptr;
-            }
+    const uint64_t cnt = gr.idx.size(), mp = gr.m_pad, np = gr.n_pad;
+    q.batch = (int)cnt;
+    q.vec_ok = 1;
+    if (kind == 0) {
+        if (!make_tmap_3d(&q.tmA, gr.X[xin], np, mp, cnt, np, mp * np, kBK, kBM, 0)) return false;
+        if (!make_tmap_3d(&q.tmB, gr.X[xin], np, mp, cnt, np, mp * np, kBK, bn, 0)) return false;
+        q.M = q.N = (int)mp;
+        q.K = (int)np;
+        q.sym = 1;
+        q.out = gr.A;
+        q.out_ld = mp;
+        q.out_bstride = mp * mp;
+        q.alpha = 1.f;
+        q.scale = it == 0 ? P.s2 + gr.zbase : nullptr;
+    } else if (kind == 1) {
+        if (!make_tmap_3d(&q.tmA, gr.A, mp, mp, cnt, mp, mp * mp, kBK, kBM, 0)) return false;
+        if (!make_tmap_3d(&q.tmB, gr.A, mp, mp, cnt, mp, mp * mp, kBK, bn, 0)) return false;
+        q.M = q.N = q.K = (int)mp;
+        q.sym = 1;
+        q.out = gr.Bm;
+        q.out_ld = mp;
+        q.out_bstride = mp * mp;
+        q.aux = gr.A;
+        q.aux_ld = mp;
+        q.aux_bstride = mp * mp;
+        q.alpha = c;
+        q.beta = b;
+    } else {
+        if (!make_tmap_3d(&q.tmA, gr.Bm, mp, mp, cnt, mp, mp * mp, kBK, kBM, 0)) return false;
+        if (!make_tmap_3d(&q.tmB, gr.X[xin], np, mp, cnt, np, mp * np, 64, kBK, 0)) return false;
+        q.b_mn = 1;
+        q.M = (int)mp;
+        q.N = (int)np;
+        q.K = (int)mp;
+        q.out = gr.X[xout];
+        q.out_ld = np;
+        q.out_bstride = mp * np;
+        q.aux = gr.X[xin];
+        q.aux_ld = np;
+        q.aux_bstride = mp * np;
+        q.alpha = 1.f;
+        q.beta = a;
+        q.scale = it == 0 ? P.s + gr.zbase : nullptr;
+    }
+    return true;
+}
+
+// All Newton-Schulz iterations: for every (up to 4) shape groups, up to 5
+// iterations (15 phases: Gram, poly, apply) per cooperative launch, with a
+// grid barrier between phases.
+mc_status run_ns_iterations(const NsPlan& P, int steps, float a, float b, float c, cudaStream_t stream) {
+    const int ngroups = (int)P.groups.size();
+    for (int g0 = 0; g0 < ngroups; g0 += 4) {
+        const int g1 = std::min(ngroups, g0 + 4);
+        const int per_launch = std::min(kMaxPhases / 3, kMaxProblemsMulti / (3 * (g1 - g0)));
+        // narrow 64-column tiles (8-stage ring) when 256-column tiles of the
+        // apply phase would leave SMs idle
+        long long apply_tiles = 0;
+        for (int g = g0; g < g1; ++g) {
+            const NsGroup& gr = P.groups[g];
+            apply_tiles += (long long)gr.idx.size() * (gr.m_pad / kBM) * ((gr.n_pad + kBN - 1) / kBN);
         }
-        static const char* kinds[3] = {"gemm:ns_gram", "gemm:ns_poly", "gemm:ns_apply"};
-        finalize_gemm_params(G);
-        MC_CUDA(launch_gemm(G, stream, kinds[kind]));
+        const int bn = apply_tiles < num_sms() ? 64 : kBN;
+        for (int it0 = 0; it0 < steps; it0 += per_launch) {
+            const int nit = std::min(per_launch, steps - it0);
+            static GemmParamsMulti G;  // ~27 KB: not on the stack; filled and launched under g_launch_mu
+            std::lock_guard<std::mutex> lk(g_launch_mu);
+            memset(&G, 0, sizeof(G));
+            G.bn = bn;
+            for (int it = it0; it < it0 + nit; ++it)
+                for (int kind = 0; kind < 3; ++kind) {
+                    G.phase_prob[G.nphase++] = G.nprob;
+                    for (int g = g0; g < g1; ++g)
+                        if (!ns_problem(G.p[G.nprob++], P, P.groups[g], kind, it, a, b, c, bn)) return MC_ERR_CUDA;
+                }
+            G.phase_prob[G.nphase] = G.nprob;
+            G.grid_bar = P.bar;
+            finalize_gemm_params(G);
+            MC_CUDA(cudaMemsetAsync(P.bar, 0, sizeof(unsigned), stream));
+            MC_CUDA(launch_gemm_multi(G, stream, "gemm:ns"));
+        }
     }
     return MC_OK;
 }
@@ -802,11 +845,7 @@ mc_status muon_impl(bool step, float* const* w, const float* const* g, float* co
                                 stream);
     if (st != MC_OK) return st;
     if ((st = run_norm(P, eps, stream)) != MC_OK) return st;
-    for (int it = 0; it < steps; ++it) {
-        if ((st = run_ns_phase(P, 0, it, a, b, c, stream)) != MC_OK) return st;
-        if ((st = run_ns_phase(P, 1, it, a, b, c, stream)) != MC_OK) return st;
-        if ((st = run_ns_phase(P, 2, it, a, b, c, stream)) != MC_OK) return st;
-    }
+    if ((st = run_ns_iterations(P, steps, a, b, c, stream)) != MC_OK) return st;
     return run_mat_pass(P, step ? 2 : 3, step ? w : out, g, m, in, rows, cols, steps & 1, mu, lr, wd, rms_coef,
                         nesterov, steps == 0, stream);
 }

@@ -17,7 +17,6 @@
 namespace mc {
 
 constexpr int kAStageBytes = kBM * kBK * 2;  // 16 KB
-constexpr int kBStageBytes = kBN * kBK * 2;  // 32 KB
 constexpr int kGemmThreads = 192;
 // epilogue staging: each epilogue warp stages a 32 x 64 chunk of 16-bit
 // values in rows of 72 elements (144 B: 16-byte accesses are bank-conflict
@@ -25,11 +24,20 @@ constexpr int kGemmThreads = 192;
 // 16-byte access by 8 lanes per 128-byte row segment
 constexpr int kStageLd = 72;
 constexpr int kEpiWarpBytes = 32 * kStageLd * 2;  // 4608 B
-constexpr int kGemmSmem = kGemmStages * (kAStageBytes + kBStageBytes) + 4 * kEpiWarpBytes + 1024 + 256;
+// Tile / pipeline shapes: BN = 256 with 4 stages of 48 KB (large problems),
+// BN = 64 with 8 stages of 24 KB (small problems: more tiles in flight per
+// phase and twice the TMA round trips in flight per SM).
+template <int BN, int STAGES>
+struct TileCfg {
+    static constexpr int kBStage = BN * kBK * 2;
+    static constexpr int kSmem = STAGES * (kAStageBytes + kBStage) + 4 * kEpiWarpBytes + 1024 + 384;
+    static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
+};
 
+template <int STAGES>
 struct GemmSmemTail {
-    uint64_t full[kGemmStages];
-    uint64_t empty[kGemmStages];
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
@@ -37,9 +45,10 @@ struct GemmSmemTail {
     int abort_flag;
 };
 
-MC_D void decode_tile(const GemmParams& P, int t, int& pi, int& z, int& tm, int& tn) {
-    pi = 0;
-    while (pi + 1 < P.nprob && t >= P.p[pi + 1].tile_begin) ++pi;
+template <int BN, int MAXP>
+MC_D void decode_tile(const GemmParamsT<MAXP>& P, int pb, int pe, int t, int& pi, int& z, int& tm, int& tn) {
+    pi = pb;
+    while (pi + 1 < pe && t >= P.p[pi + 1].tile_begin) ++pi;
     const GemmProblem& q = P.p[pi];
     int local = t - q.tile_begin;
     z = local / q.tiles_per_batch;
@@ -48,18 +57,51 @@ MC_D void decode_tile(const GemmParams& P, int t, int& pi, int& z, int& tm, int&
         tm = r / q.tiles_n;
         tn = r - tm * q.tiles_n;
     } else {
-        // row block tm holds the tiles tn >= tm/2 (those touching c >= r)
+        // row block tm holds the tiles tn >= 128 tm / BN (those touching c >= r)
         tm = 0;
         while (true) {
-            int cnt = q.tiles_n - (tm >> 1);
+            const int first = (kBM * tm) / BN;
+            int cnt = q.tiles_n - first;
             if (r < cnt) {
-                tn = (tm >> 1) + r;
+                tn = first + r;
                 break;
             }
             r -= cnt;
             ++tm;
         }
     }
+}
+
+// Grid-wide barrier between phases of a multi-phase (cooperative) launch:
+// every CTA's phase stores are released (gpu scope, and to the async proxy
+// that the next phase's TMA loads use) before any CTA proceeds.  Bounded.
+template <int MAXP>
+MC_D void grid_sync(const GemmParamsT<MAXP>& P, int ph, volatile int* abort_flag) {
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        atomicAdd(P.grid_bar, 1u);
+        const unsigned target = (unsigned)(ph + 1) * gridDim.x;
+        uint64_t t0 = 0;
+        while (true) {
+            unsigned v;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(P.grid_bar) : "memory");
+            if (v >= target) break;
+            if (t0 == 0) {
+                t0 = globaltimer_ns();
+            } else if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                set_status(P.status, MC_DEV_TIMEOUT);
+                break;
+            }
+            __nanosleep(32);
+        }
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+    __syncthreads();
+    tc_fence_after();
 }
 
 MC_D void store_bf16x8(__nv_bfloat16* dst, const float* v) {
@@ -291,13 +333,17 @@ MC_D void epilogue_chunk_staged(const GemmProblem& q, int z, int row0, int col0,
     }
 }
 
-__global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParams P) {
+template <int MAXP, int BN, int STAGES>
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParamsT<MAXP> P) {
+    using Cfg = TileCfg<BN, STAGES>;
+    constexpr int kBStageBytes = Cfg::kBStage;
+    constexpr int kGemmStages = STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + kGemmStages * kAStageBytes;
     uint16_t* sEpi = reinterpret_cast<uint16_t*>(sB + kGemmStages * kBStageBytes);
-    GemmSmemTail* tail = reinterpret_cast<GemmSmemTail*>(sB + kGemmStages * kBStageBytes + 4 * kEpiWarpBytes);
+    auto* tail = reinterpret_cast<GemmSmemTail<STAGES>*>(sB + kGemmStages * kBStageBytes + 4 * kEpiWarpBytes);
     volatile int* abort_flag = &tail->abort_flag;
 
     const int warp = threadIdx.x >> 5;
@@ -323,7 +369,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         }
     }
     if (warp == 1) {
-        tmem_alloc(&tail->tmem_base, 512);
+        tmem_alloc(&tail->tmem_base, Cfg::kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -332,160 +378,212 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     const uint32_t tmem_base = tail->tmem_base;
     pdl_wait();  // the previous kernel's outputs are our inputs
 
-    if (warp == 0) {
-        // ---------------- TMA producer ----------------
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t issued[kGemmStages] = {0, 0, 0, 0};
-            bool ok = true;
-            for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
+    // role state, carried across phases
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, aphase = 0;
+    uint32_t issued[STAGES];
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) issued[s] = 0;
+    bool ok = true;
+
+    for (int ph = 0; ph < P.nphase; ++ph) {
+        const int pb = P.phase_prob[ph], pe = P.phase_prob[ph + 1];
+        const int t_begin = P.p[pb].tile_begin;
+        const int t_end = pe < P.nprob ? P.p[pe].tile_begin : P.total_tiles;
+        ok = ok && !*abort_flag;
+        if (warp == 0) {
+            // ---------------- TMA producer ----------------
+            if (lane == 0 && ok) {
+                for (int t = t_begin + blockIdx.x; t < t_end && ok; t += gridDim.x) {
+                    int pi, z, tm, tn;
+                    decode_tile<BN>(P, pb, pe, t, pi, z, tm, tn);
+                    const GemmProblem& q = P.p[pi];
+                    const int nk = (q.K + kBK - 1) / kBK;
+                    for (int kb = 0; kb < nk; ++kb) {
+                        if (!mbar_wait(&tail->empty[stage], phase ^ 1, abort_flag, P.status)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&tail->full[stage], kAStageBytes + kBStageBytes);
+                        tma_load_3d(sA + stage * kAStageBytes, &q.tmA, &tail->full[stage], kb * kBK,
+                                    tm * kBM, z);
+                        uint8_t* b = sB + stage * kBStageBytes;
+                        if (!q.b_mn) {
+                            tma_load_3d(b, &q.tmB, &tail->full[stage], kb * kBK, tn * BN, z);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < BN / 64; ++j)
+                                tma_load_3d(b + j * (kBK * 128), &q.tmB, &tail->full[stage],
+                                            tn * BN + j * 64, kb * kBK, z);
+                        }
+                        ++issued[stage];
+                        if (++stage == kGemmStages) {
+                            stage = 0;
+                            phase ^= 1;
+                        }
+                    }
+                }
+            }
+        } else if (warp == 1) {
+            // ---------------- MMA issuer ----------------
+            for (int t = t_begin + blockIdx.x; t < t_end && ok; t += gridDim.x) {
                 int pi, z, tm, tn;
-                decode_tile(P, t, pi, z, tm, tn);
+                decode_tile<BN>(P, pb, pe, t, pi, z, tm, tn);
                 const GemmProblem& q = P.p[pi];
                 const int nk = (q.K + kBK - 1) / kBK;
+                const uint32_t idesc = idesc_f16kind(kBM, BN, q.b_mn, q.ab_f16);
+                if (!mbar_wait(&tail->tempty[acc], aphase ^ 1, abort_flag, P.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 for (int kb = 0; kb < nk; ++kb) {
-                    if (!mbar_wait(&tail->empty[stage], phase ^ 1, abort_flag, P.status)) {
+                    if (!mbar_wait(&tail->full[stage], phase, abort_flag, P.status)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&tail->full[stage], kAStageBytes + kBStageBytes);
-                    tma_load_3d(sA + stage * kAStageBytes, &q.tmA, &tail->full[stage], kb * kBK,
-                                tm * kBM, z);
-                    uint8_t* b = sB + stage * kBStageBytes;
-                    if (!q.b_mn) {
-                        tma_load_3d(b, &q.tmB, &tail->full[stage], kb * kBK, tn * kBN, z);
-                    } else {
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t a0 = smem_u32(sA + stage * kAStageBytes);
+                        const uint32_t b0 = smem_u32(sB + stage * kBStageBytes);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            tma_load_3d(b + j * (kBK * 128), &q.tmB, &tail->full[stage],
-                                        tn * kBN + j * 64, kb * kBK, z);
+                        for (int k = 0; k < kBK / 16; ++k) {
+                            uint64_t ad = sw128_desc(a0 + k * 32, 16, 1024);
+                            uint64_t bd = q.b_mn ? sw128_desc(b0 + k * 2048, kBK * 128, 1024)
+                                                 : sw128_desc(b0 + k * 32, 16, 1024);
+                            umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0);
+                        }
+                        umma_commit(&tail->empty[stage]);
                     }
-                    ++issued[stage];
+                    __syncwarp();
                     if (++stage == kGemmStages) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
-            }
-            // wait for this thread's copies still in flight before exit
-            for (int s = 0; s < kGemmStages; ++s)
-                if (issued[s]) {
-                    volatile int never = 0;
-                    mbar_wait(&tail->full[s], (issued[s] - 1) & 1, &never, P.status);
+                if (!ok) break;
+                if (lane == 0) umma_commit(&tail->tfull[acc]);
+                __syncwarp();
+                if (++acc == 2) {
+                    acc = 0;
+                    aphase ^= 1;
                 }
-        }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        int stage = 0, acc = 0;
-        uint32_t phase = 0, aphase = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; t < P.total_tiles && ok; t += gridDim.x) {
-            int pi, z, tm, tn;
-            decode_tile(P, t, pi, z, tm, tn);
-            const GemmProblem& q = P.p[pi];
-            const int nk = (q.K + kBK - 1) / kBK;
-            const uint32_t idesc = idesc_f16kind(kBM, kBN, q.b_mn, q.ab_f16);
-            if (!mbar_wait(&tail->tempty[acc], aphase ^ 1, abort_flag, P.status)) break;
-            tc_fence_after();
-            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
-            for (int kb = 0; kb < nk; ++kb) {
-                if (!mbar_wait(&tail->full[stage], phase, abort_flag, P.status)) {
+            }
+        } else {
+            // ---------------- epilogue (warps 2..5) ----------------
+            const int quarter = warp & 3;  // TMEM lanes this warp may access
+            uint16_t* S = sEpi + (warp - 2) * (32 * kStageLd);
+            for (int t = t_begin + blockIdx.x; t < t_end && ok; t += gridDim.x) {
+                int pi, z, tm, tn;
+                decode_tile<BN>(P, pb, pe, t, pi, z, tm, tn);
+                const GemmProblem& q = P.p[pi];
+                if (!mbar_wait(&tail->tfull[acc], aphase, abort_flag, P.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t a0 = smem_u32(sA + stage * kAStageBytes);
-                    const uint32_t b0 = smem_u32(sB + stage * kBStageBytes);
-#pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k) {
-                        uint64_t ad = sw128_desc(a0 + k * 32, 16, 1024);
-                        uint64_t bd = q.b_mn ? sw128_desc(b0 + k * 2048, kBK * 128, 1024)
-                                             : sw128_desc(b0 + k * 32, 16, 1024);
-                        umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0);
-                    }
-                    umma_commit(&tail->empty[stage]);
+                const int row0 = tm * kBM + quarter * 32;
+                const int r = row0 + lane;
+                const float sc = q.scale ? q.scale[z] : 1.0f;
+                const bool staged = q.vec_ok && q.out_kind != kOutF32;
+#pragma unroll 1
+                for (int c = 0; c < BN / 64; ++c) {
+                    uint32_t v[64];
+                    uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + c * 64);
+                    tmem_ld32(taddr, v);
+                    tmem_ld32(taddr + 32, v + 32);
+                    tmem_ld_wait();
+                    if (staged)
+                        epilogue_chunk_staged(q, z, row0, tn * BN + c * 64, reinterpret_cast<float*>(v), sc, S,
+                                              P.status);
+                    else
+                        epilogue_chunk(q, z, r, tn * BN + c * 64, reinterpret_cast<float*>(v), sc, P.status);
                 }
+                tc_fence_before();
                 __syncwarp();
-                if (++stage == kGemmStages) {
-                    stage = 0;
-                    phase ^= 1;
+                if (lane == 0) mbar_arrive(&tail->tempty[acc]);
+                if (++acc == 2) {
+                    acc = 0;
+                    aphase ^= 1;
                 }
-            }
-            if (!ok) break;
-            if (lane == 0) umma_commit(&tail->tfull[acc]);
-            __syncwarp();
-            if (++acc == 2) {
-                acc = 0;
-                aphase ^= 1;
             }
         }
+        if (ph + 1 < P.nphase) grid_sync(P, ph, abort_flag);
+    }
+
+    if (warp == 0 && lane == 0) {
+        // wait for this thread's copies still in flight before exit
+        volatile int never = 0;
+        for (int s = 0; s < kGemmStages; ++s)
+            if (issued[s]) mbar_wait(&tail->full[s], (issued[s] - 1) & 1, &never, P.status);
+    } else if (warp == 1) {
         // drain: every MMA this thread issued has completed before teardown
         if (lane == 0) umma_commit(&tail->drain);
         __syncwarp();
         volatile int never = 0;
         mbar_wait(&tail->drain, 0, &never, P.status);
-    } else {
-        // ---------------- epilogue (warps 2..5) ----------------
-        const int quarter = warp & 3;  // TMEM lanes this warp may access
-        int acc = 0;
-        uint32_t aphase = 0;
-        for (int t = blockIdx.x; t < P.total_tiles; t += gridDim.x) {
-            int pi, z, tm, tn;
-            decode_tile(P, t, pi, z, tm, tn);
-            const GemmProblem& q = P.p[pi];
-            if (!mbar_wait(&tail->tfull[acc], aphase, abort_flag, P.status)) break;
-            tc_fence_after();
-            const int row0 = tm * kBM + quarter * 32;
-            const int r = row0 + lane;
-            const float sc = q.scale ? q.scale[z] : 1.0f;
-            const bool staged = q.vec_ok && q.out_kind != kOutF32;
-            uint16_t* S = sEpi + (warp - 2) * (32 * kStageLd);
-#pragma unroll 1
-            for (int c = 0; c < kBN / 64; ++c) {
-                uint32_t v[64];
-                uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN + c * 64);
-                tmem_ld32(taddr, v);
-                tmem_ld32(taddr + 32, v + 32);
-                tmem_ld_wait();
-                if (staged)
-                    epilogue_chunk_staged(q, z, row0, tn * kBN + c * 64, reinterpret_cast<float*>(v), sc, S,
-                                          P.status);
-                else
-                    epilogue_chunk(q, z, r, tn * kBN + c * 64, reinterpret_cast<float*>(v), sc, P.status);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tail->tempty[acc]);
-            if (++acc == 2) {
-                acc = 0;
-                aphase ^= 1;
-            }
-        }
     }
 
     pdl_trigger();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, 512);
+    if (warp == 1) tmem_dealloc(tmem_base, Cfg::kTmemCols);
 }
 
-cudaError_t launch_gemm(const GemmParams& P, cudaStream_t stream, const char* label) {
-    if (P.total_tiles <= 0) return cudaSuccess;
+template <int MAXP, int BN, int STAGES>
+static cudaError_t set_smem_attr() {
     static bool attr_set[64] = {false};
     int dev = current_device();
     if (dev < 0) return cudaErrorInvalidDevice;
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<MAXP, BN, STAGES>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<BN, STAGES>::kSmem);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
+    return cudaSuccess;
+}
+
+cudaError_t launch_gemm(const GemmParams& P, cudaStream_t stream, const char* label) {
+    if (P.total_tiles <= 0) return cudaSuccess;
+    if (P.bn != kBN) return cudaErrorInvalidValue;
+    cudaError_t e = set_smem_attr<kMaxProblems, kBN, kGemmStages>();
+    if (e != cudaSuccess) return e;
     int grid = num_sms();
     if (grid > P.total_tiles) grid = P.total_tiles;
     TraceScope ts(label, stream);
-    return launch_pdl(gemm_kernel, dim3(grid), dim3(kGemmThreads), kGemmSmem, stream, P);
+    return launch_pdl(gemm_kernel<kMaxProblems, kBN, kGemmStages>, dim3(grid), dim3(kGemmThreads),
+                      TileCfg<kBN, kGemmStages>::kSmem, stream, P);
+}
+
+// All phases in one cooperative launch: one CTA per SM, every CTA resident,
+// grid barriers between phases.
+template <int BN, int STAGES>
+static cudaError_t launch_multi_cfg(const GemmParamsMulti& P, cudaStream_t stream, const char* label) {
+    cudaError_t e = set_smem_attr<kMaxProblemsMulti, BN, STAGES>();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms());
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = TileCfg<BN, STAGES>::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    TraceScope ts(label, stream);
+    e = cudaLaunchKernelEx(&cfg, gemm_kernel<kMaxProblemsMulti, BN, STAGES>, P);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_gemm_multi(const GemmParamsMulti& P, cudaStream_t stream, const char* label) {
+    if (P.total_tiles <= 0) return cudaSuccess;
+    if (P.bn == 64) return launch_multi_cfg<64, 8>(P, stream, label);
+    if (P.bn == kBN) return launch_multi_cfg<kBN, kGemmStages>(P, stream, label);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace mc

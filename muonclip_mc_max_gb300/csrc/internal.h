@@ -20,7 +20,9 @@ constexpr int kBM = 128;  // UMMA M (TMEM lanes)
 constexpr int kBN = 256;  // UMMA N (TMEM columns per accumulator)
 constexpr int kBK = 64;   // K per smem stage: one 128-byte swizzle row of bf16
 constexpr int kGemmStages = 4;
-constexpr int kMaxProblems = 4;
+constexpr int kMaxProblems = 4;        // problems of a single-phase launch
+constexpr int kMaxProblemsMulti = 60;  // problems of a multi-phase launch
+constexpr int kMaxPhases = 16;
 
 // One GEMM problem of a multi-problem launch: D[z] = A[z] * op(B[z]),
 // A [M][K] K-major; B K-major ([N][K]) or MN-major ([K][N]).
@@ -48,11 +50,22 @@ struct GemmProblem {
     int rope_T, rope_period, rope_start, pad_;
 };
 
-struct GemmParams {
-    GemmProblem p[kMaxProblems];
+// A launch: problems in tile order.  With nphase > 1 the problems form
+// consecutive phases (phase i = problems [phase_prob[i], phase_prob[i+1]));
+// every CTA finishes its tiles of a phase before any CTA starts the next
+// (grid barrier on *grid_bar, a zeroed counter; cooperative launch).
+template <int MAXP>
+struct GemmParamsT {
+    GemmProblem p[MAXP];
     int nprob, total_tiles;
+    int bn;  // output tile width of the launch: 256 (default when 0) or 64
+    int nphase;
+    int phase_prob[kMaxPhases + 1];
+    unsigned* grid_bar;
     unsigned* status;
 };
+using GemmParams = GemmParamsT<kMaxProblems>;
+using GemmParamsMulti = GemmParamsT<kMaxProblemsMulti>;
 
 // ---------------------------------------------------------------------------
 // helpers (abi.cu)
@@ -80,11 +93,14 @@ bool make_tmap_3d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t ou
                   uint64_t batch, uint64_t outer_stride, uint64_t batch_stride,
                   uint32_t box_inner, uint32_t box_outer, int f16);
 
-// Fills the tile bookkeeping of problems [0, nprob) and total_tiles.
-void finalize_gemm_params(GemmParams& P);
+// Fills the tile bookkeeping of problems [0, nprob), total_tiles and (when
+// nphase is 0) a single phase.
+template <int MAXP>
+void finalize_gemm_params(GemmParamsT<MAXP>& P);
 
 // gemm.cu
 cudaError_t launch_gemm(const GemmParams& P, cudaStream_t stream, const char* label);
+cudaError_t launch_gemm_multi(const GemmParamsMulti& P, cudaStream_t stream, const char* label);
 
 // scan.cu
 struct ScanArgs {
