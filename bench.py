@@ -62,9 +62,7 @@ def scan_pairs(B, T, causal):
 # which their traffic grows in proportion to.  Drop an entry whenever the
 # kernel changes after the capture.
 TRAFFIC = {
-    ("c2", "scan"): 33599488,
-    ("c4", "muon_momentum"): 3758299648 + 2768514048,
-    ("c3", "scan"): int((231511296 + 3700224) * 16),
+    ("c2", "scan"): 33611520,
 }
 
 

@@ -305,7 +305,7 @@ static size_t mha_carve(Carve& c, int B, int T, int D, int H, int dh, mc_dtype d
         *q = c.take<float>(n);
         *k = c.take<float>(n);
     }
-    *keys = c.take<unsigned>((size_t)B * H);
+    *keys = c.take<unsigned>((size_t)B * H + 1);  // + the scan's done-counter
     return c.used;
 }
 
@@ -331,7 +331,7 @@ mc_status mc_max_logits_mha(const void* x, const void* wq, const void* wk, mc_dt
     void *q, *k;
     unsigned* keys;
     mha_carve(c, B, T, D, H, dh, dtype, &q, &k, &keys);
-    MC_CUDA(cudaMemsetAsync(keys, 0, sizeof(unsigned) * B * H, stream));
+    MC_CUDA(cudaMemsetAsync(keys, 0, sizeof(unsigned) * ((size_t)B * H + 1), stream));
     const int64_t BT = (int64_t)B * T, N = (int64_t)H * dh;
     if (mha_tensor_path(dtype, D, dh)) {
         if (!aligned16(x) || !aligned16(wq) || !aligned16(wk)) return MC_ERR_INVALID_ARG;
@@ -357,13 +357,17 @@ mc_status mc_max_logits_mha(const void* x, const void* wq, const void* wk, mc_dt
         a.nkb_main = dh / 64;
         a.nkb_rope = 0;
         a.keys = keys;
-        MC_CUDA(launch_scan(a, stream));
+        a.d = (float)dh;
+        a.accumulate = accumulate;
+        a.s_max = s_max;
+        a.s_bh = s_max_bh;
+        MC_CUDA(launch_scan(a, stream));  // finalises S_max in its last CTA
     } else {
         MC_CUDA(launch_proj_simt(x, wq, dtype, (float*)q, (int)BT, D, (int)N, stream));
         MC_CUDA(launch_proj_simt(x, wk, dtype, (float*)k, (int)BT, D, (int)N, stream));
         MC_CUDA(launch_scan_simt((const float*)q, (const float*)k, B, T, H, dh, causal ? 1 : 0, keys, stream));
+        MC_CUDA(launch_finalize_smax(keys, B, H, (float)dh, accumulate, s_max, s_max_bh, stream));
     }
-    MC_CUDA(launch_finalize_smax(keys, B, H, (float)dh, accumulate, s_max, s_max_bh, stream));
     return MC_OK;
 }
 
@@ -430,7 +434,7 @@ static size_t mla_carve(Carve& c, const mc_mla_layer* L, int B, int T, MlaWs& w)
     w.kc = c.take<__half>(BT * (size_t)L->H * L->nope);
     w.wqb = c.take<__half>((size_t)L->q_lora * L->H * (L->nope + L->rope));
     w.wkb = c.take<__half>((size_t)L->kv_lora * L->H * L->nope);
-    w.keys = c.take<unsigned>((size_t)B * L->H);
+    w.keys = c.take<unsigned>((size_t)B * L->H + 1);  // + the scan's done-counter
     return c.used;
 }
 
@@ -457,7 +461,7 @@ mc_status mc_max_logits_mla(const mc_mla_layer* L, const void* x, int B, int T, 
     mla_carve(c, L, B, T, w);
     const int64_t BT = (int64_t)B * T;
     const int qk = L->nope + L->rope, kvw = L->kv_lora + L->rope;
-    MC_CUDA(cudaMemsetAsync(w.keys, 0, sizeof(unsigned) * B * L->H, stream));
+    MC_CUDA(cudaMemsetAsync(w.keys, 0, sizeof(unsigned) * ((size_t)B * L->H + 1), stream));
     MC_CUDA(launch_rope_table(w.rope, T, L->rope_base, stream));
     // phase 1: c_Q = x W_qa ; [c_KV | k^R] = x W_kva (RoPE on the k^R columns)
     GemmParams P;
@@ -508,8 +512,11 @@ mc_status mc_max_logits_mla(const mc_mla_layer* L, const void* x, int B, int T, 
     a.nkb_rope = 1;
     a.kr_col = L->kv_lora;
     a.keys = w.keys;
-    MC_CUDA(launch_scan(a, stream));
-    MC_CUDA(launch_finalize_smax(w.keys, B, L->H, (float)qk, accumulate, s_max, s_max_bh, stream));
+    a.d = (float)qk;
+    a.accumulate = accumulate;
+    a.s_max = s_max;
+    a.s_bh = s_max_bh;
+    MC_CUDA(launch_scan(a, stream));  // finalises S_max in its last CTA
     return MC_OK;
 }
 
@@ -602,6 +609,7 @@ struct NsPlan {
     float* s;
     float* s2;
     unsigned* bar;  // grid-barrier counter of the multi-phase launches
+    MatInfo* info;  // per-matrix facts, written by the momentum pass
     size_t bytes;
 };
 
@@ -648,6 +656,7 @@ bool plan_ns(const int* rows, const int* cols, int count, uint8_t* base, NsPlan&
     P.s = c.take<float>(count);
     P.s2 = c.take<float>(count);
     P.bar = c.take<unsigned>(1);
+    P.info = c.take<MatInfo>(count);
     P.bytes = c.used;
     return true;
 }
@@ -682,6 +691,8 @@ mc_status run_mat_pass(const NsPlan& P, int mode, float* const* w, const float* 
         B.lr = lr;
         B.wd = wd;
         B.nesterov = nesterov;
+        B.info = mode <= 1 ? P.info : nullptr;
+        B.info_base = c0;
         int tiles = 0;
         for (int p = c0; p < std::min(count, c0 + kMaxBatchMats); ++p) {
             const int i = P.order[p];
@@ -697,14 +708,14 @@ mc_status run_mat_pass(const NsPlan& P, int mode, float* const* w, const float* 
             d.tiles_x = gr.n_pad / 64;
             d.tile_begin = tiles;
             tiles += (gr.m_pad / 64) * (gr.n_pad / 64);
+            d.w = w[i];
+            d.rms = rms_coef * sqrtf((float)std::max(rows[i], cols[i]));
             if (mode == 0) {
                 d.m = m[i];
                 d.g = g[i];
             } else if (mode == 1) {
                 d.m = const_cast<float*>(in[i]);
             } else {
-                d.w = w[i];
-                d.rms = rms_coef * sqrtf((float)std::max(rows[i], cols[i]));
                 d.oscale = zero_steps ? P.s + p : nullptr;
             }
         }
@@ -788,19 +799,20 @@ bool ns_problem(GemmProblem& q, const NsPlan& P, const NsGroup& gr, int kind, in
 // All Newton-Schulz iterations: for every (up to 4) shape groups, up to 5
 // iterations (15 phases: Gram, poly, apply) per cooperative launch, with a
 // grid barrier between phases.
-mc_status run_ns_iterations(const NsPlan& P, int steps, float a, float b, float c, cudaStream_t stream) {
+mc_status run_ns_iterations(const NsPlan& P, int steps, float a, float b, float c, float eps,
+                            cudaStream_t stream) {
     const int ngroups = (int)P.groups.size();
     for (int g0 = 0; g0 < ngroups; g0 += 4) {
         const int g1 = std::min(ngroups, g0 + 4);
         const int per_launch = std::min(kMaxPhases / 3, kMaxProblemsMulti / (3 * (g1 - g0)));
-        // narrow 64-column tiles (8-stage ring) when 256-column tiles of the
-        // apply phase would leave SMs idle
+        // 128-column tiles (6-stage ring) when 256-column tiles of the apply
+        // phase would leave SMs idle
         long long apply_tiles = 0;
         for (int g = g0; g < g1; ++g) {
             const NsGroup& gr = P.groups[g];
             apply_tiles += (long long)gr.idx.size() * (gr.m_pad / kBM) * ((gr.n_pad + kBN - 1) / kBN);
         }
-        const int bn = apply_tiles < num_sms() ? 64 : kBN;
+        const int bn = apply_tiles < num_sms() ? 128 : kBN;
         for (int it0 = 0; it0 < steps; it0 += per_launch) {
             const int nit = std::min(per_launch, steps - it0);
             static GemmParamsMulti G;  // ~27 KB: not on the stack; filled and launched under g_launch_mu
@@ -815,6 +827,14 @@ mc_status run_ns_iterations(const NsPlan& P, int steps, float a, float b, float 
                 }
             G.phase_prob[G.nphase] = G.nprob;
             G.grid_bar = P.bar;
+            G.mats = P.info;
+            G.s = P.s;
+            G.s2 = P.s2;
+            G.eps = eps;
+            if (it0 == 0) {  // first launch of this chunk: the norm pre-phase
+                G.norm_begin = P.groups[g0].zbase;
+                G.norm_end = P.groups[g1 - 1].zbase + (int)P.groups[g1 - 1].idx.size();
+            }
             finalize_gemm_params(G);
             MC_CUDA(cudaMemsetAsync(P.bar, 0, sizeof(unsigned), stream));
             MC_CUDA(launch_gemm_multi(G, stream, "gemm:ns"));
@@ -841,11 +861,16 @@ mc_status muon_impl(bool step, float* const* w, const float* const* g, float* co
     plan_ns(rows, cols, count, nullptr, P);
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < P.bytes) return MC_ERR_WORKSPACE;
     plan_ns(rows, cols, count, (uint8_t*)ws, P);
-    mc_status st = run_mat_pass(P, step ? 0 : 1, w, g, m, in, rows, cols, 0, mu, lr, wd, rms_coef, nesterov, false,
-                                stream);
+    mc_status st = run_mat_pass(P, step ? 0 : 1, step ? w : out, g, m, in, rows, cols, 0, mu, lr, wd, rms_coef,
+                                nesterov, false, stream);
     if (st != MC_OK) return st;
-    if ((st = run_norm(P, eps, stream)) != MC_OK) return st;
-    if ((st = run_ns_iterations(P, steps, a, b, c, stream)) != MC_OK) return st;
+    // the norm runs as the pre-phase of the first Newton-Schulz launch; with
+    // zero steps it is a launch of its own and the update applies the scale
+    if (steps > 0)
+        st = run_ns_iterations(P, steps, a, b, c, eps, stream);
+    else
+        st = run_norm(P, eps, stream);
+    if (st != MC_OK) return st;
     return run_mat_pass(P, step ? 2 : 3, step ? w : out, g, m, in, rows, cols, steps & 1, mu, lr, wd, rms_coef,
                         nesterov, steps == 0, stream);
 }

@@ -201,6 +201,14 @@ __global__ void __launch_bounds__(kMatThreads) mat_pass_kernel(const __grid_cons
     __shared__ double red[kMatThreads / 32];
     const int tid = threadIdx.x;
     pdl_wait();
+    if (B.info && B.mode <= 1 && blockIdx.x == 0 && tid < B.count) {
+        const MatDesc& d = B.d[tid];
+        MatInfo mi;
+        mi.partial = d.partial;
+        mi.nparts = (d.m_pad / kTile) * (d.n_pad / kTile);
+        mi.pad_ = 0;
+        B.info[B.info_base + tid] = mi;
+    }
     for (int t = blockIdx.x; t < B.total_tiles; t += gridDim.x) {
         int di;
         find_mat(B, t, di);

@@ -25,8 +25,8 @@ constexpr int kGemmThreads = 192;
 constexpr int kStageLd = 72;
 constexpr int kEpiWarpBytes = 32 * kStageLd * 2;  // 4608 B
 // Tile / pipeline shapes: BN = 256 with 4 stages of 48 KB (large problems),
-// BN = 64 with 8 stages of 24 KB (small problems: more tiles in flight per
-// phase and twice the TMA round trips in flight per SM).
+// BN = 128 with 6 stages of 32 KB (small Newton-Schulz batches: twice the
+// tiles per phase, so more SMs share each phase, and more stages in flight).
 template <int BN, int STAGES>
 struct TileCfg {
     static constexpr int kBStage = BN * kBK * 2;
@@ -76,14 +76,14 @@ MC_D void decode_tile(const GemmParamsT<MAXP>& P, int pb, int pe, int t, int& pi
 // every CTA's phase stores are released (gpu scope, and to the async proxy
 // that the next phase's TMA loads use) before any CTA proceeds.  Bounded.
 template <int MAXP>
-MC_D void grid_sync(const GemmParamsT<MAXP>& P, int ph, volatile int* abort_flag) {
+MC_D void grid_sync(const GemmParamsT<MAXP>& P, int seq, volatile int* abort_flag) {
     tc_fence_before();
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
         asm volatile("fence.proxy.async.global;" ::: "memory");
         atomicAdd(P.grid_bar, 1u);
-        const unsigned target = (unsigned)(ph + 1) * gridDim.x;
+        const unsigned target = (unsigned)(seq + 1) * gridDim.x;
         uint64_t t0 = 0;
         while (true) {
             unsigned v;
@@ -233,12 +233,11 @@ MC_D uint4 pack8(const float* v, bool f16) {
 // back into S, then written with coalesced 16-byte stores: the rows, and for
 // symmetric outputs the mirrored rows (c, r) of every c >= r.  Only the
 // 16-byte segment that straddles the diagonal is written element-wise.
-MC_D void epilogue_chunk_staged(const GemmProblem& q, int z, int row0, int col0, float* f, float sc,
-                                uint16_t* S, unsigned* status) {
+// The chunk's values: RoPE, then v = sc (alpha acc + beta aux) with aux
+// rows fetched by coalesced 16-byte loads through the staging buffer S.
+MC_D void chunk_values(const GemmProblem& q, int z, int row0, int col0, float* f, float sc, uint16_t* S) {
     const int lane = threadIdx.x & 31;
     const int r = row0 + lane;
-    if (col0 >= q.N) return;  // warp-uniform
-    __syncwarp();             // every lane is done with the previous chunk's S
     const int seg = lane & 7, sub = lane >> 3;
     if (q.rope_tab && (col0 % q.rope_period) == q.rope_start && r < q.M) {
         const float2* cs = q.rope_tab + (size_t)(r % q.rope_T) * 32;
@@ -280,6 +279,15 @@ MC_D void epilogue_chunk_staged(const GemmProblem& q, int z, int row0, int col0,
 #pragma unroll
         for (int i = 0; i < 64; ++i) f[i] *= s2;
     }
+}
+
+MC_D void epilogue_chunk_staged(const GemmProblem& q, int z, int row0, int col0, float* f, float sc,
+                                uint16_t* S, unsigned* status) {
+    const int lane = threadIdx.x & 31;
+    if (col0 >= q.N) return;  // warp-uniform
+    __syncwarp();             // every lane is done with the previous chunk's S
+    const int seg = lane & 7, sub = lane >> 3;
+    chunk_values(q, z, row0, col0, f, sc, S);
     const bool f16 = q.out_kind == kOutF16;
     if (f16) {
         bool big = false;
@@ -330,6 +338,28 @@ MC_D void epilogue_chunk_staged(const GemmProblem& q, int z, int row0, int col0,
             for (int i = 0; i < 8; ++i)
                 if (r0 + i <= c) dst[i] = e[i];
         }
+    }
+}
+
+// Pre-phase of a multi-phase Newton-Schulz launch: s = 1 / (||U||_F + eps)
+// and s^2 from the momentum pass's per-tile sums of squares, one matrix per
+// CTA at a time, summed in a fixed order.
+template <int MAXP>
+MC_D void norm_prephase(const GemmParamsT<MAXP>& P, double* red) {
+    for (int z = P.norm_begin + blockIdx.x; z < P.norm_end; z += gridDim.x) {
+        const MatInfo& mi = P.mats[z];
+        double acc = 0.0;
+        for (int i = threadIdx.x; i < mi.nparts; i += blockDim.x) acc += mi.partial[i];
+        red[threadIdx.x] = acc;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            double tot = 0.0;
+            for (int i = 0; i < (int)blockDim.x; ++i) tot += red[i];
+            const double den = sqrt(tot) + (double)P.eps;
+            P.s[z] = (float)(1.0 / den);
+            P.s2[z] = (float)(1.0 / (den * den));
+        }
+        __syncthreads();
     }
 }
 
@@ -385,6 +415,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) issued[s] = 0;
     bool ok = true;
+    int nsync = 0;
+    if (P.norm_end > P.norm_begin) {
+        norm_prephase(P, reinterpret_cast<double*>(sEpi));
+        grid_sync(P, nsync++, abort_flag);
+    }
 
     for (int ph = 0; ph < P.nphase; ++ph) {
         const int pb = P.phase_prob[ph], pe = P.phase_prob[ph + 1];
@@ -509,7 +544,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 }
             }
         }
-        if (ph + 1 < P.nphase) grid_sync(P, ph, abort_flag);
+        if (ph + 1 < P.nphase) grid_sync(P, nsync++, abort_flag);
     }
 
     if (warp == 0 && lane == 0) {
@@ -581,7 +616,7 @@ static cudaError_t launch_multi_cfg(const GemmParamsMulti& P, cudaStream_t strea
 
 cudaError_t launch_gemm_multi(const GemmParamsMulti& P, cudaStream_t stream, const char* label) {
     if (P.total_tiles <= 0) return cudaSuccess;
-    if (P.bn == 64) return launch_multi_cfg<64, 8>(P, stream, label);
+    if (P.bn == 128) return launch_multi_cfg<128, 6>(P, stream, label);
     if (P.bn == kBN) return launch_multi_cfg<kBN, kGemmStages>(P, stream, label);
     return cudaErrorInvalidValue;
 }

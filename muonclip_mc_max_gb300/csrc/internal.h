@@ -50,6 +50,14 @@ struct GemmProblem {
     int rope_T, rope_period, rope_start, pad_;
 };
 
+// Per-matrix facts of a Muon batch, written to the workspace by the
+// momentum pass and read by the norm pre-phase of the multi-phase
+// Newton-Schulz launch.
+struct MatInfo {
+    const double* partial;   // per-tile sums of squares of the Newton-Schulz input
+    int nparts, pad_;
+};
+
 // A launch: problems in tile order.  With nphase > 1 the problems form
 // consecutive phases (phase i = problems [phase_prob[i], phase_prob[i+1]));
 // every CTA finishes its tiles of a phase before any CTA starts the next
@@ -63,6 +71,12 @@ struct GemmParamsT {
     int phase_prob[kMaxPhases + 1];
     unsigned* grid_bar;
     unsigned* status;
+    // multi-phase Newton-Schulz extras
+    const MatInfo* mats;
+    int norm_begin, norm_end;  // pre-phase: s, s2 of matrices [norm_begin, norm_end)
+    float eps;
+    float* s;
+    float* s2;
 };
 using GemmParams = GemmParamsT<kMaxProblems>;
 using GemmParamsMulti = GemmParamsT<kMaxProblemsMulti>;
@@ -118,7 +132,12 @@ struct ScanArgs {
     int nkb_main;        // 64-wide K blocks per head read from K main
     int nkb_rope;        // 0 or 1 block read from k^R at column kr_col
     int kr_col;
-    unsigned* keys;      // [B*H] monotonic keys (max-merged)
+    unsigned* keys;      // [B*H] monotonic keys (max-merged), then a zeroed done-counter
+    // finalisation, done by the last CTA to finish: S = key / sqrt(d)
+    float d;
+    int accumulate;
+    float* s_max;
+    float* s_bh;
 };
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream);
 
@@ -177,6 +196,8 @@ struct MatDesc {
 };
 struct MatBatch {
     MatDesc d[kMaxBatchMats];
+    MatInfo* info;  // modes 0/1: info[info_base + i] is written for matrix i
+    int info_base;
     int count, total_tiles;
     float mu, lr, wd;
     int nesterov, mode;  // 0 momentum + cast, 1 cast only, 2 update W, 3 write O

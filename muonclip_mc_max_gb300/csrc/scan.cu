@@ -40,6 +40,11 @@ struct ScanParams {
     int q_head_stride, k_head_stride, nkb_main, nkb_rope, kr_col;
     int n_it, total_items;
     unsigned* keys;
+    unsigned* done;  // zeroed counter of finished CTAs
+    float sqrt_d;
+    int accumulate;
+    float* s_max;
+    float* s_bh;
     unsigned* status;
 };
 
@@ -52,7 +57,24 @@ struct ScanSmemTail {
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
+    int last_cta;
 };
+
+// S_max[h] = max over sequences of key / sqrt(d) (NaN propagates); the
+// per-sequence maxima are written too when s_bh is given.
+MC_D void finalize_head(const unsigned* keys, int B, int H, int h, float sqrt_d, int accumulate,
+                        float* s_max, float* s_bh, unsigned* status) {
+    unsigned best = 0;
+    for (int b = 0; b < B; ++b) {
+        unsigned k = __ldcg(keys + b * H + h);
+        if (s_bh) s_bh[b * H + h] = __fdiv_rn(key_float(k), sqrt_d);
+        best = max(best, k);
+    }
+    float s = __fdiv_rn(key_float(best), sqrt_d);
+    if (accumulate) s = max_nan(s_max[h], s);
+    if (!isfinite(s)) set_status(status, MC_DEV_NONFINITE);
+    s_max[h] = s;
+}
 
 MC_D void decode_item(const ScanParams& P, int i, int& b, int& h, int& it, int& njt) {
     const int BH = P.B * P.H;
@@ -279,6 +301,20 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(const __grid_cons
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, 512);
+
+    // the last CTA to finish turns the keys into S_max (threadfence pattern:
+    // every CTA's atomics are visible before its count is)
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned old = atomicAdd(P.done, 1u);
+        tail->last_cta = old == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (tail->last_cta) {
+        __threadfence();
+        for (int h = threadIdx.x; h < P.H; h += blockDim.x)
+            finalize_head(P.keys, P.B, P.H, h, P.sqrt_d, P.accumulate, P.s_max, P.s_bh, P.status);
+    }
 }
 
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream) {
@@ -309,6 +345,11 @@ cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream) {
     P.n_it = (a.T + kBM - 1) / kBM;
     P.total_items = a.B * a.H * P.n_it;
     P.keys = a.keys;
+    P.done = a.keys + (size_t)a.B * a.H;
+    P.sqrt_d = sqrtf(a.d);
+    P.accumulate = a.accumulate;
+    P.s_max = a.s_max;
+    P.s_bh = a.s_bh;
     P.status = device_status_ptr();
     static bool attr_set[64] = {false};
     int dev = current_device();
@@ -401,16 +442,7 @@ __global__ void finalize_smax_kernel(const unsigned* __restrict__ keys, int B, i
     pdl_wait();
     int h = blockIdx.x * blockDim.x + threadIdx.x;
     if (h >= H) return;
-    unsigned best = 0;
-    for (int b = 0; b < B; ++b) {
-        unsigned k = keys[b * H + h];
-        if (s_bh) s_bh[b * H + h] = __fdiv_rn(key_float(k), sqrt_d);
-        best = max(best, k);
-    }
-    float s = __fdiv_rn(key_float(best), sqrt_d);
-    if (accumulate) s = max_nan(s_max[h], s);
-    if (!isfinite(s)) set_status(status, MC_DEV_NONFINITE);
-    s_max[h] = s;
+    finalize_head(keys, B, H, h, sqrt_d, accumulate, s_max, s_bh, status);
     pdl_trigger();
 }
 
