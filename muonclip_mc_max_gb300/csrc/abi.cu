@@ -744,9 +744,12 @@ mc_status run_norm(const NsPlan& P, float eps, cudaStream_t stream) {
 }
 
 // One Newton-Schulz GEMM of iteration `it` for a shape group:
-// kind 0: Gram A = sc2 X X^T ; 1: poly B = c A A + b A ; 2: apply X' = sc (B X + a X)
+// kind 0: Gram A = sc2 X X^T ; 1: poly B = c A A + b A ; 2: apply X' = sc (B X + a X).
+// sym: Gram and poly compute the tiles on and above the diagonal and mirror
+// them (exactly symmetric A, B); otherwise every tile is computed, which
+// costs no time when the full tiling still fits the same number of waves.
 bool ns_problem(GemmProblem& q, const NsPlan& P, const NsGroup& gr, int kind, int it, float a, float b,
-                float c, int bn) {
+                float c, int bn, int sym) {
     memset(&q, 0, sizeof(q));
     const int xin = it & 1, xout = (it + 1) & 1;
     const uint64_t cnt = gr.idx.size(), mp = gr.m_pad, np = gr.n_pad;
@@ -757,7 +760,7 @@ bool ns_problem(GemmProblem& q, const NsPlan& P, const NsGroup& gr, int kind, in
         if (!make_tmap_3d(&q.tmB, gr.X[xin], np, mp, cnt, np, mp * np, kBK, bn, 0)) return false;
         q.M = q.N = (int)mp;
         q.K = (int)np;
-        q.sym = 1;
+        q.sym = sym;
         q.out = gr.A;
         q.out_ld = mp;
         q.out_bstride = mp * mp;
@@ -767,7 +770,7 @@ bool ns_problem(GemmProblem& q, const NsPlan& P, const NsGroup& gr, int kind, in
         if (!make_tmap_3d(&q.tmA, gr.A, mp, mp, cnt, mp, mp * mp, kBK, kBM, 0)) return false;
         if (!make_tmap_3d(&q.tmB, gr.A, mp, mp, cnt, mp, mp * mp, kBK, bn, 0)) return false;
         q.M = q.N = q.K = (int)mp;
-        q.sym = 1;
+        q.sym = sym;
         q.out = gr.Bm;
         q.out_ld = mp;
         q.out_bstride = mp * mp;
@@ -813,6 +816,18 @@ mc_status run_ns_iterations(const NsPlan& P, int steps, float a, float b, float 
             apply_tiles += (long long)gr.idx.size() * (gr.m_pad / kBM) * ((gr.n_pad + kBN - 1) / kBN);
         }
         const int bn = apply_tiles < num_sms() ? 128 : kBN;
+        // full Gram / poly tilings when they take no more waves than the symmetric ones
+        long long sym_tiles = 0, full_tiles = 0;
+        for (int g = g0; g < g1; ++g) {
+            const NsGroup& gr = P.groups[g];
+            const long long tm = gr.m_pad / kBM, tn = (gr.m_pad + bn - 1) / bn;
+            long long t = 0;
+            for (long long i = 0; i < tm; ++i) t += tn - (kBM * i) / bn;
+            sym_tiles += (long long)gr.idx.size() * t;
+            full_tiles += (long long)gr.idx.size() * tm * tn;
+        }
+        const long long nsm = num_sms();
+        const int sym = (full_tiles + nsm - 1) / nsm > (sym_tiles + nsm - 1) / nsm ? 1 : 0;
         for (int it0 = 0; it0 < steps; it0 += per_launch) {
             const int nit = std::min(per_launch, steps - it0);
             static GemmParamsMulti G;  // ~27 KB: not on the stack; filled and launched under g_launch_mu
@@ -823,7 +838,8 @@ mc_status run_ns_iterations(const NsPlan& P, int steps, float a, float b, float 
                 for (int kind = 0; kind < 3; ++kind) {
                     G.phase_prob[G.nphase++] = G.nprob;
                     for (int g = g0; g < g1; ++g)
-                        if (!ns_problem(G.p[G.nprob++], P, P.groups[g], kind, it, a, b, c, bn)) return MC_ERR_CUDA;
+                        if (!ns_problem(G.p[G.nprob++], P, P.groups[g], kind, it, a, b, c, bn, sym))
+                            return MC_ERR_CUDA;
                 }
             G.phase_prob[G.nphase] = G.nprob;
             G.grid_bar = P.bar;

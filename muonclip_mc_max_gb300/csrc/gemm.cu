@@ -27,10 +27,18 @@ constexpr int kEpiWarpBytes = 32 * kStageLd * 2;  // 4608 B
 // Tile / pipeline shapes: BN = 256 with 4 stages of 48 KB (large problems),
 // BN = 128 with 6 stages of 32 KB (small Newton-Schulz batches: twice the
 // tiles per phase, so more SMs share each phase, and more stages in flight).
+// Shared-memory copies of the current and the next phase's problems: the
+// roles read the problem fields from here instead of the (large, dynamically
+// indexed) kernel parameters, whose constant-cache misses would otherwise sit
+// on every phase's critical path.  TMA still reads the tensor maps from the
+// parameters.
+constexpr int kTailBytes = 384;
+constexpr int kProbStageBytes = 2 * kPhaseProbs * (int)sizeof(GemmProblem);
 template <int BN, int STAGES>
 struct TileCfg {
     static constexpr int kBStage = BN * kBK * 2;
-    static constexpr int kSmem = STAGES * (kAStageBytes + kBStage) + 4 * kEpiWarpBytes + 1024 + 384;
+    static constexpr int kSmem = STAGES * (kAStageBytes + kBStage) + 4 * kEpiWarpBytes + 1024 + kTailBytes +
+                                 64 + kProbStageBytes;
     static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
 };
 
@@ -45,11 +53,13 @@ struct GemmSmemTail {
     int abort_flag;
 };
 
-template <int BN, int MAXP>
-MC_D void decode_tile(const GemmParamsT<MAXP>& P, int pb, int pe, int t, int& pi, int& z, int& tm, int& tn) {
-    pi = pb;
-    while (pi + 1 < pe && t >= P.p[pi + 1].tile_begin) ++pi;
-    const GemmProblem& q = P.p[pi];
+// Tile t of a phase -> (problem index within the phase, batch, row block,
+// column block); sp holds the phase's np problems.
+template <int BN>
+MC_D void decode_tile(const GemmProblem* sp, int np, int t, int& pi, int& z, int& tm, int& tn) {
+    pi = 0;
+    while (pi + 1 < np && t >= sp[pi + 1].tile_begin) ++pi;
+    const GemmProblem& q = sp[pi];
     int local = t - q.tile_begin;
     z = local / q.tiles_per_batch;
     int r = local - z * q.tiles_per_batch;
@@ -72,13 +82,27 @@ MC_D void decode_tile(const GemmParamsT<MAXP>& P, int pb, int pe, int t, int& pi
     }
 }
 
+// Copy phase ph's problems from the kernel parameters into shared memory
+// (16-byte pieces spread over threads tid0.. of the CTA).
+template <int MAXP>
+MC_D void stage_phase(const GemmParamsT<MAXP>& P, int ph, GemmProblem* dst, int tid, int nthr) {
+    const int pb = P.phase_prob[ph], pe = P.phase_prob[ph + 1];
+    const uint4* src = reinterpret_cast<const uint4*>(&P.p[pb]);
+    uint4* d = reinterpret_cast<uint4*>(dst);
+    const int n = (pe - pb) * (int)(sizeof(GemmProblem) / 16);
+    for (int i = tid; i < n; i += nthr) d[i] = src[i];
+}
+
 // Grid-wide barrier between phases of a multi-phase (cooperative) launch:
 // every CTA's phase stores are released (gpu scope, and to the async proxy
 // that the next phase's TMA loads use) before any CTA proceeds.  Bounded.
 template <int MAXP>
-MC_D void grid_sync(const GemmParamsT<MAXP>& P, int seq, volatile int* abort_flag) {
+MC_D void grid_sync(const GemmParamsT<MAXP>& P, int seq, volatile int* abort_flag, int next_ph,
+                    GemmProblem* next_dst) {
     tc_fence_before();
     __syncthreads();
+    // the other threads stage the next phase's problems while thread 0 waits
+    if (next_ph >= 0 && threadIdx.x >= 32) stage_phase(P, next_ph, next_dst, threadIdx.x - 32, blockDim.x - 32);
     if (threadIdx.x == 0) {
         __threadfence();
         asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -374,6 +398,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     uint8_t* sB = smem + kGemmStages * kAStageBytes;
     uint16_t* sEpi = reinterpret_cast<uint16_t*>(sB + kGemmStages * kBStageBytes);
     auto* tail = reinterpret_cast<GemmSmemTail<STAGES>*>(sB + kGemmStages * kBStageBytes + 4 * kEpiWarpBytes);
+    static_assert(sizeof(GemmSmemTail<STAGES>) <= kTailBytes, "tail");
+    GemmProblem* sProb = reinterpret_cast<GemmProblem*>(
+        (reinterpret_cast<uintptr_t>(tail) + kTailBytes + 63) & ~uintptr_t(63));
     volatile int* abort_flag = &tail->abort_flag;
 
     const int warp = threadIdx.x >> 5;
@@ -402,6 +429,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         tmem_alloc(&tail->tmem_base, Cfg::kTmemCols);
         tmem_relinquish();
     }
+    if (warp >= 2) stage_phase(P, 0, sProb, threadIdx.x - 64, blockDim.x - 64);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -418,21 +446,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     int nsync = 0;
     if (P.norm_end > P.norm_begin) {
         norm_prephase(P, reinterpret_cast<double*>(sEpi));
-        grid_sync(P, nsync++, abort_flag);
+        grid_sync(P, nsync++, abort_flag, -1, nullptr);
     }
 
     for (int ph = 0; ph < P.nphase; ++ph) {
-        const int pb = P.phase_prob[ph], pe = P.phase_prob[ph + 1];
-        const int t_begin = P.p[pb].tile_begin;
-        const int t_end = pe < P.nprob ? P.p[pe].tile_begin : P.total_tiles;
+        const int pb = P.phase_prob[ph], np = P.phase_prob[ph + 1] - pb;
+        const GemmProblem* sp = sProb + (ph & 1) * kPhaseProbs;
+        const int t_begin = sp[0].tile_begin;
+        const int t_end = sp[np - 1].tile_begin + sp[np - 1].tiles_per_batch * sp[np - 1].batch;
         ok = ok && !*abort_flag;
         if (warp == 0) {
             // ---------------- TMA producer ----------------
             if (lane == 0 && ok) {
                 for (int t = t_begin + blockIdx.x; t < t_end && ok; t += gridDim.x) {
                     int pi, z, tm, tn;
-                    decode_tile<BN>(P, pb, pe, t, pi, z, tm, tn);
-                    const GemmProblem& q = P.p[pi];
+                    decode_tile<BN>(sp, np, t, pi, z, tm, tn);
+                    const GemmProblem& q = sp[pi];
+                    const CUtensorMap* tmA = &P.p[pb + pi].tmA;
+                    const CUtensorMap* tmB = &P.p[pb + pi].tmB;
                     const int nk = (q.K + kBK - 1) / kBK;
                     for (int kb = 0; kb < nk; ++kb) {
                         if (!mbar_wait(&tail->empty[stage], phase ^ 1, abort_flag, P.status)) {
@@ -440,16 +471,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                             break;
                         }
                         mbar_arrive_expect_tx(&tail->full[stage], kAStageBytes + kBStageBytes);
-                        tma_load_3d(sA + stage * kAStageBytes, &q.tmA, &tail->full[stage], kb * kBK,
-                                    tm * kBM, z);
+                        tma_load_3d(sA + stage * kAStageBytes, tmA, &tail->full[stage], kb * kBK, tm * kBM, z);
                         uint8_t* b = sB + stage * kBStageBytes;
                         if (!q.b_mn) {
-                            tma_load_3d(b, &q.tmB, &tail->full[stage], kb * kBK, tn * BN, z);
+                            tma_load_3d(b, tmB, &tail->full[stage], kb * kBK, tn * BN, z);
                         } else {
 #pragma unroll
                             for (int j = 0; j < BN / 64; ++j)
-                                tma_load_3d(b + j * (kBK * 128), &q.tmB, &tail->full[stage],
-                                            tn * BN + j * 64, kb * kBK, z);
+                                tma_load_3d(b + j * (kBK * 128), tmB, &tail->full[stage], tn * BN + j * 64,
+                                            kb * kBK, z);
                         }
                         ++issued[stage];
                         if (++stage == kGemmStages) {
@@ -463,8 +493,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             // ---------------- MMA issuer ----------------
             for (int t = t_begin + blockIdx.x; t < t_end && ok; t += gridDim.x) {
                 int pi, z, tm, tn;
-                decode_tile<BN>(P, pb, pe, t, pi, z, tm, tn);
-                const GemmProblem& q = P.p[pi];
+                decode_tile<BN>(sp, np, t, pi, z, tm, tn);
+                const GemmProblem& q = sp[pi];
                 const int nk = (q.K + kBK - 1) / kBK;
                 const uint32_t idesc = idesc_f16kind(kBM, BN, q.b_mn, q.ab_f16);
                 if (!mbar_wait(&tail->tempty[acc], aphase ^ 1, abort_flag, P.status)) {
@@ -511,8 +541,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             uint16_t* S = sEpi + (warp - 2) * (32 * kStageLd);
             for (int t = t_begin + blockIdx.x; t < t_end && ok; t += gridDim.x) {
                 int pi, z, tm, tn;
-                decode_tile<BN>(P, pb, pe, t, pi, z, tm, tn);
-                const GemmProblem& q = P.p[pi];
+                decode_tile<BN>(sp, np, t, pi, z, tm, tn);
+                const GemmProblem& q = sp[pi];
                 if (!mbar_wait(&tail->tfull[acc], aphase, abort_flag, P.status)) {
                     ok = false;
                     break;
@@ -544,7 +574,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 }
             }
         }
-        if (ph + 1 < P.nphase) grid_sync(P, nsync++, abort_flag);
+        if (ph + 1 < P.nphase) grid_sync(P, nsync++, abort_flag, ph + 1, sProb + ((ph + 1) & 1) * kPhaseProbs);
     }
 
     if (warp == 0 && lane == 0) {
@@ -581,9 +611,20 @@ static cudaError_t set_smem_attr() {
     return cudaSuccess;
 }
 
+// every phase holds 1..kPhaseProbs problems (the shared-memory staging size)
+template <int MAXP>
+static bool phases_fit(const GemmParamsT<MAXP>& P) {
+    if (P.nphase < 1 || P.nphase > kMaxPhases) return false;
+    for (int ph = 0; ph < P.nphase; ++ph) {
+        const int n = P.phase_prob[ph + 1] - P.phase_prob[ph];
+        if (n < 1 || n > kPhaseProbs) return false;
+    }
+    return P.phase_prob[P.nphase] == P.nprob;
+}
+
 cudaError_t launch_gemm(const GemmParams& P, cudaStream_t stream, const char* label) {
     if (P.total_tiles <= 0) return cudaSuccess;
-    if (P.bn != kBN) return cudaErrorInvalidValue;
+    if (P.bn != kBN || !phases_fit(P)) return cudaErrorInvalidValue;
     cudaError_t e = set_smem_attr<kMaxProblems, kBN, kGemmStages>();
     if (e != cudaSuccess) return e;
     int grid = num_sms();
@@ -616,6 +657,7 @@ static cudaError_t launch_multi_cfg(const GemmParamsMulti& P, cudaStream_t strea
 
 cudaError_t launch_gemm_multi(const GemmParamsMulti& P, cudaStream_t stream, const char* label) {
     if (P.total_tiles <= 0) return cudaSuccess;
+    if (!phases_fit(P)) return cudaErrorInvalidValue;
     if (P.bn == 128) return launch_multi_cfg<128, 6>(P, stream, label);
     if (P.bn == kBN) return launch_multi_cfg<kBN, kGemmStages>(P, stream, label);
     return cudaErrorInvalidValue;

@@ -23,6 +23,7 @@ constexpr int kGemmStages = 4;
 constexpr int kMaxProblems = 4;        // problems of a single-phase launch
 constexpr int kMaxProblemsMulti = 60;  // problems of a multi-phase launch
 constexpr int kMaxPhases = 16;
+constexpr int kPhaseProbs = 4;  // problems per phase (staged in shared memory)
 
 // One GEMM problem of a multi-problem launch: D[z] = A[z] * op(B[z]),
 // A [M][K] K-major; B K-major ([N][K]) or MN-major ([K][N]).
