@@ -71,7 +71,8 @@ static EncodeTiledFn encode_fn() {
 }
 
 bool make_tmap_3d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, uint64_t batch,
-                  uint64_t outer_stride, uint64_t batch_stride, uint32_t box_inner, uint32_t box_outer, int f16) {
+                  uint64_t outer_stride, uint64_t batch_stride, uint32_t box_inner, uint32_t box_outer, int f16,
+                  bool swizzle) {
     EncodeTiledFn fn = encode_fn();
     if (!fn || !base || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
     if (batch == 1) batch_stride = outer_stride * outer;
@@ -81,7 +82,8 @@ bool make_tmap_3d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t ou
     cuuint32_t box[3] = {box_inner, box_outer, 1};
     cuuint32_t es[3] = {1, 1, 1};
     CUresult r = fn(tm, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -755,6 +757,13 @@ bool ns_problem(GemmProblem& q, const NsPlan& P, const NsGroup& gr, int kind, in
     const uint64_t cnt = gr.idx.size(), mp = gr.m_pad, np = gr.n_pad;
     q.batch = (int)cnt;
     q.vec_ok = 1;
+    // workspace buffers: 256-byte aligned, rows of m_pad / n_pad (multiples of 64) elements
+    q.bulk_st = kind == 2 || !sym;
+    if (q.bulk_st) {
+        const void* out = kind == 0 ? (const void*)gr.A : kind == 1 ? (const void*)gr.Bm : (const void*)gr.X[xout];
+        const uint64_t on = kind == 2 ? np : mp;
+        if (!make_tmap_3d(&q.tmC, out, on, mp, cnt, on, mp * on, 64, 32, 0, false)) return false;
+    }
     if (kind == 0) {
         if (!make_tmap_3d(&q.tmA, gr.X[xin], np, mp, cnt, np, mp * np, kBK, kBM, 0)) return false;
         if (!make_tmap_3d(&q.tmB, gr.X[xin], np, mp, cnt, np, mp * np, kBK, bn, 0)) return false;

@@ -251,15 +251,26 @@ MC_D uint4 pack8(const float* v, bool f16) {
     return u;
 }
 
-// Warp-cooperative epilogue of a 32-row x 64-column chunk (rows row0.., one
-// per lane; 16-bit output with vec_ok).  Aux rows are fetched with coalesced
-// 16-byte loads into the warp's staging buffer S, the results are staged
-// back into S, then written with coalesced 16-byte stores: the rows, and for
-// symmetric outputs the mirrored rows (c, r) of every c >= r.  Only the
-// 16-byte segment that straddles the diagonal is written element-wise.
-// The chunk's values: RoPE, then v = sc (alpha acc + beta aux) with aux
-// rows fetched by coalesced 16-byte loads through the staging buffer S.
-MC_D void chunk_values(const GemmProblem& q, int z, int row0, int col0, float* f, float sc, uint16_t* S) {
+// Aux rows of a 32-row x 64-column chunk, one 16-byte segment per lane and
+// pass (4 rows x 8 segments per pass): coalesced, issued early so that the
+// loads are in flight while the accumulator is still being produced.
+MC_D void aux_load(const GemmProblem& q, int z, int row0, int col0, uint4 (&u)[8]) {
+    const int lane = threadIdx.x & 31;
+    const int seg = lane & 7, sub = lane >> 3;
+    const __nv_bfloat16* ab = q.aux + (size_t)z * q.aux_bstride + col0 + seg * 8;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int grow = row0 + it * 4 + sub;
+        u[it] = (grow < q.M && col0 + seg * 8 < q.N) ? *reinterpret_cast<const uint4*>(ab + (size_t)grow * q.aux_ld)
+                                                     : make_uint4(0, 0, 0, 0);
+    }
+}
+
+// The chunk's values: RoPE, then v = sc (alpha acc + beta aux) with the aux
+// segments u (from aux_load) transposed to one row per lane through the
+// warp's staging buffer S.
+MC_D void chunk_values(const GemmProblem& q, int row0, int col0, float* f, float sc, uint16_t* S,
+                       const uint4 (&u)[8]) {
     const int lane = threadIdx.x & 31;
     const int r = row0 + lane;
     const int seg = lane & 7, sub = lane >> 3;
@@ -274,15 +285,6 @@ MC_D void chunk_values(const GemmProblem& q, int z, int row0, int col0, float* f
         }
     }
     if (q.aux) {
-        const __nv_bfloat16* ab = q.aux + (size_t)z * q.aux_bstride + col0 + seg * 8;
-        uint4 u[8];
-#pragma unroll
-        for (int it = 0; it < 8; ++it) {
-            const int rr = it * 4 + sub, grow = row0 + rr;
-            u[it] = (grow < q.M && col0 + seg * 8 < q.N)
-                        ? *reinterpret_cast<const uint4*>(ab + (size_t)grow * q.aux_ld)
-                        : make_uint4(0, 0, 0, 0);
-        }
 #pragma unroll
         for (int it = 0; it < 8; ++it) *reinterpret_cast<uint4*>(S + (it * 4 + sub) * kStageLd + seg * 8) = u[it];
         __syncwarp();
@@ -305,13 +307,26 @@ MC_D void chunk_values(const GemmProblem& q, int z, int row0, int col0, float* f
     }
 }
 
+// Warp-cooperative epilogue of a 32-row x 64-column chunk (rows row0.., one
+// per lane; 16-bit output with vec_ok).  The results are staged in the
+// warp's buffer S and written either by one TMA tensor store of the whole
+// chunk (bulk_st: one request instead of one per row or segment, which is
+// what limits the write rate of a few warps) or by coalesced 16-byte
+// stores: the rows, and for symmetric
+// outputs the mirrored rows (c, r) of every c >= r, where only the 16-byte
+// segment that straddles the diagonal is written element-wise.  With
+// next_col0 >= 0 the next chunk's aux rows are loaded into u once this
+// chunk's are consumed.
 MC_D void epilogue_chunk_staged(const GemmProblem& q, int z, int row0, int col0, float* f, float sc,
-                                uint16_t* S, unsigned* status) {
+                                uint16_t* S, unsigned* status, uint4 (&u)[8], int next_col0,
+                                const CUtensorMap* tmC) {
     const int lane = threadIdx.x & 31;
     if (col0 >= q.N) return;  // warp-uniform
-    __syncwarp();             // every lane is done with the previous chunk's S
+    bulk_wait_read();  // this lane's bulk copies out of S (if any) have read it
+    __syncwarp();      // every lane is done with the previous chunk's S
     const int seg = lane & 7, sub = lane >> 3;
-    chunk_values(q, z, row0, col0, f, sc, S);
+    chunk_values(q, row0, col0, f, sc, S, u);
+    if (q.aux && next_col0 >= 0 && next_col0 < q.N) aux_load(q, z, row0, next_col0, u);
     const bool f16 = q.out_kind == kOutF16;
     if (f16) {
         bool big = false;
@@ -319,10 +334,22 @@ MC_D void epilogue_chunk_staged(const GemmProblem& q, int z, int row0, int col0,
         for (int i = 0; i < 64; ++i) big |= fabsf(f[i]) > 65504.0f;
         if (big) set_status(status, MC_DEV_RANGE);
     }
+    if (q.bulk_st) {
+        // dense 32 x 64 box (128-byte rows) for the tensor store
+#pragma unroll
+        for (int v = 0; v < 8; ++v) *reinterpret_cast<uint4*>(S + lane * 64 + v * 8) = pack8(f + 8 * v, f16);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_3d(tmC, S, col0, row0, z);
+            bulk_commit();
+        }
+        return;
+    }
 #pragma unroll
     for (int v = 0; v < 8; ++v) *reinterpret_cast<uint4*>(S + lane * kStageLd + v * 8) = pack8(f + 8 * v, f16);
-    __syncwarp();
     uint16_t* ob = reinterpret_cast<uint16_t*>(q.out) + (size_t)z * q.out_bstride;
+    __syncwarp();
     // rows: 8 passes of 4 rows x 8 segments
 #pragma unroll
     for (int it = 0; it < 8; ++it) {
@@ -423,6 +450,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         for (int i = 0; i < P.nprob; ++i) {
             tma_prefetch_desc(&P.p[i].tmA);
             tma_prefetch_desc(&P.p[i].tmB);
+            if (P.p[i].bulk_st) tma_prefetch_desc(&P.p[i].tmC);
         }
     }
     if (warp == 1) {
@@ -543,6 +571,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 int pi, z, tm, tn;
                 decode_tile<BN>(sp, np, t, pi, z, tm, tn);
                 const GemmProblem& q = sp[pi];
+                const bool staged = q.vec_ok && q.out_kind != kOutF32;
+                uint4 u[8] = {};
+                if (staged && q.aux) aux_load(q, z, tm * kBM + quarter * 32, tn * BN, u);
                 if (!mbar_wait(&tail->tfull[acc], aphase, abort_flag, P.status)) {
                     ok = false;
                     break;
@@ -551,7 +582,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 const int row0 = tm * kBM + quarter * 32;
                 const int r = row0 + lane;
                 const float sc = q.scale ? q.scale[z] : 1.0f;
-                const bool staged = q.vec_ok && q.out_kind != kOutF32;
 #pragma unroll 1
                 for (int c = 0; c < BN / 64; ++c) {
                     uint32_t v[64];
@@ -561,7 +591,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                     tmem_ld_wait();
                     if (staged)
                         epilogue_chunk_staged(q, z, row0, tn * BN + c * 64, reinterpret_cast<float*>(v), sc, S,
-                                              P.status);
+                                              P.status, u, c + 1 < BN / 64 ? tn * BN + (c + 1) * 64 : -1,
+                                              &P.p[pb + pi].tmC);
                     else
                         epilogue_chunk(q, z, r, tn * BN + c * 64, reinterpret_cast<float*>(v), sc, P.status);
                 }
@@ -573,6 +604,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                     aphase ^= 1;
                 }
             }
+            // this lane's bulk copies are written before the phase ends
+            bulk_wait_all();
+            asm volatile("fence.proxy.async.global;" ::: "memory");
         }
         if (ph + 1 < P.nphase) grid_sync(P, nsync++, abort_flag, ph + 1, sProb + ((ph + 1) & 1) * kPhaseProbs);
     }
@@ -611,6 +645,7 @@ static cudaError_t set_smem_attr() {
     return cudaSuccess;
 }
 
+static_assert(sizeof(GemmParamsMulti) <= 32764, "kernel parameters");
 // every phase holds 1..kPhaseProbs problems (the shared-memory staging size)
 template <int MAXP>
 static bool phases_fit(const GemmParamsT<MAXP>& P) {

@@ -21,7 +21,7 @@ constexpr int kBN = 256;  // UMMA N (TMEM columns per accumulator)
 constexpr int kBK = 64;   // K per smem stage: one 128-byte swizzle row of bf16
 constexpr int kGemmStages = 4;
 constexpr int kMaxProblems = 4;        // problems of a single-phase launch
-constexpr int kMaxProblemsMulti = 60;  // problems of a multi-phase launch
+constexpr int kMaxProblemsMulti = 48;  // problems of a multi-phase launch (kernel parameters < 32 KB)
 constexpr int kMaxPhases = 16;
 constexpr int kPhaseProbs = 4;  // problems per phase (staged in shared memory)
 
@@ -37,9 +37,11 @@ constexpr int kOutBF16 = 0, kOutF32 = 1, kOutF16 = 2;
 struct GemmProblem {
     CUtensorMap tmA;  // 3D {K, M, batch}, box {64, 128}, 128B swizzle
     CUtensorMap tmB;  // K-major {K, N, batch} box {64, 256}; MN-major {N, K, batch} box {64, 64}
+    CUtensorMap tmC;  // bulk_st: the 16-bit output {N, M, batch}, box {64, 32}, no swizzle
     int M, N, K, batch;
     int b_mn, sym, out_kind, vec_ok;  // out_kind: kOutBF16 / kOutF32 / kOutF16
-    int ab_f16, pad0_;
+    int ab_f16;
+    int bulk_st;  // non-symmetric 16-bit output written by TMA tensor stores through tmC
     int tiles_m, tiles_n, tiles_per_batch, tile_begin;
     void* out;
     long long out_ld, out_bstride;
@@ -106,7 +108,8 @@ private:
 // {box_inner, box_outer, 1}.  false on failure.
 bool make_tmap_3d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer,
                   uint64_t batch, uint64_t outer_stride, uint64_t batch_stride,
-                  uint32_t box_inner, uint32_t box_outer, int f16);
+                  uint32_t box_inner, uint32_t box_outer, int f16,
+                  bool swizzle = true);
 
 // Fills the tile bookkeeping of problems [0, nprob), total_tiles and (when
 // nphase is 0) a single phase.
