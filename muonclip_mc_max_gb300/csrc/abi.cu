@@ -762,7 +762,7 @@ bool ns_problem(GemmProblem& q, const NsPlan& P, const NsGroup& gr, int kind, in
     if (q.bulk_st) {
         const void* out = kind == 0 ? (const void*)gr.A : kind == 1 ? (const void*)gr.Bm : (const void*)gr.X[xout];
         const uint64_t on = kind == 2 ? np : mp;
-        if (!make_tmap_3d(&q.tmC, out, on, mp, cnt, on, mp * on, 64, 32, 0, false)) return false;
+        if (!make_tmap_3d(&q.tmC, out, on, mp, cnt, on, mp * on, 64, 32, 0)) return false;
     }
     if (kind == 0) {
         if (!make_tmap_3d(&q.tmA, gr.X[xin], np, mp, cnt, np, mp * np, kBK, kBM, 0)) return false;

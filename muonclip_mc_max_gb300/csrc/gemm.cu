@@ -23,7 +23,16 @@ constexpr int kGemmThreads = 192;
 // free) so that every global load/store of the epilogue is a coalesced
 // 16-byte access by 8 lanes per 128-byte row segment
 constexpr int kStageLd = 72;
-constexpr int kEpiWarpBytes = 32 * kStageLd * 2;  // 4608 B
+// 5 KB per warp (1 KB aligned): also holds a dense 32 x 64 box in the 128-byte
+// swizzled layout of the TMA tensor store
+constexpr int kEpiWarpBytes = 5120;
+static_assert(kEpiWarpBytes >= 32 * kStageLd * 2 && kEpiWarpBytes % 1024 == 0, "staging buffer");
+
+// Offset (16-bit elements) of 16-byte segment v of row r in a warp's staging
+// buffer: rows of kStageLd elements (padded: conflict-free), or swizzled
+// 128-byte rows (segment v stored at v ^ (r mod 8): conflict-free and the
+// layout a SWIZZLE_128B tensor map reads).
+MC_D int stage_off(bool swz, int r, int v) { return swz ? r * 64 + ((v ^ (r & 7)) << 3) : r * kStageLd + (v << 3); }
 // Tile / pipeline shapes: BN = 256 with 4 stages of 48 KB (large problems),
 // BN = 128 with 6 stages of 32 KB (small Newton-Schulz batches: twice the
 // tiles per phase, so more SMs share each phase, and more stages in flight).
@@ -270,7 +279,7 @@ MC_D void aux_load(const GemmProblem& q, int z, int row0, int col0, uint4 (&u)[8
 // segments u (from aux_load) transposed to one row per lane through the
 // warp's staging buffer S.
 MC_D void chunk_values(const GemmProblem& q, int row0, int col0, float* f, float sc, uint16_t* S,
-                       const uint4 (&u)[8]) {
+                       const uint4 (&u)[8], bool swz) {
     const int lane = threadIdx.x & 31;
     const int r = row0 + lane;
     const int seg = lane & 7, sub = lane >> 3;
@@ -286,11 +295,11 @@ MC_D void chunk_values(const GemmProblem& q, int row0, int col0, float* f, float
     }
     if (q.aux) {
 #pragma unroll
-        for (int it = 0; it < 8; ++it) *reinterpret_cast<uint4*>(S + (it * 4 + sub) * kStageLd + seg * 8) = u[it];
+        for (int it = 0; it < 8; ++it) *reinterpret_cast<uint4*>(S + stage_off(swz, it * 4 + sub, seg)) = u[it];
         __syncwarp();
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
-            uint4 w = *reinterpret_cast<const uint4*>(S + lane * kStageLd + v * 8);
+            uint4 w = *reinterpret_cast<const uint4*>(S + stage_off(swz, lane, v));
             const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -325,7 +334,7 @@ MC_D void epilogue_chunk_staged(const GemmProblem& q, int z, int row0, int col0,
     bulk_wait_read();  // this lane's bulk copies out of S (if any) have read it
     __syncwarp();      // every lane is done with the previous chunk's S
     const int seg = lane & 7, sub = lane >> 3;
-    chunk_values(q, row0, col0, f, sc, S, u);
+    chunk_values(q, row0, col0, f, sc, S, u, q.bulk_st != 0);
     if (q.aux && next_col0 >= 0 && next_col0 < q.N) aux_load(q, z, row0, next_col0, u);
     const bool f16 = q.out_kind == kOutF16;
     if (f16) {
@@ -335,9 +344,10 @@ MC_D void epilogue_chunk_staged(const GemmProblem& q, int z, int row0, int col0,
         if (big) set_status(status, MC_DEV_RANGE);
     }
     if (q.bulk_st) {
-        // dense 32 x 64 box (128-byte rows) for the tensor store
+        // the 32 x 64 box in the swizzled layout of the tensor store (each
+        // lane rewrites only the segments of its own row that it read)
 #pragma unroll
-        for (int v = 0; v < 8; ++v) *reinterpret_cast<uint4*>(S + lane * 64 + v * 8) = pack8(f + 8 * v, f16);
+        for (int v = 0; v < 8; ++v) *reinterpret_cast<uint4*>(S + stage_off(true, lane, v)) = pack8(f + 8 * v, f16);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -566,7 +576,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         } else {
             // ---------------- epilogue (warps 2..5) ----------------
             const int quarter = warp & 3;  // TMEM lanes this warp may access
-            uint16_t* S = sEpi + (warp - 2) * (32 * kStageLd);
+            uint16_t* S = sEpi + (warp - 2) * (kEpiWarpBytes / 2);
             for (int t = t_begin + blockIdx.x; t < t_end && ok; t += gridDim.x) {
                 int pi, z, tm, tn;
                 decode_tile<BN>(sp, np, t, pi, z, tm, tn);

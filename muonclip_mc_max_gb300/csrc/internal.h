@@ -37,7 +37,7 @@ constexpr int kOutBF16 = 0, kOutF32 = 1, kOutF16 = 2;
 struct GemmProblem {
     CUtensorMap tmA;  // 3D {K, M, batch}, box {64, 128}, 128B swizzle
     CUtensorMap tmB;  // K-major {K, N, batch} box {64, 256}; MN-major {N, K, batch} box {64, 64}
-    CUtensorMap tmC;  // bulk_st: the 16-bit output {N, M, batch}, box {64, 32}, no swizzle
+    CUtensorMap tmC;  // bulk_st: the 16-bit output {N, M, batch}, box {64, 32}, 128B swizzle
     int M, N, K, batch;
     int b_mn, sym, out_kind, vec_ok;  // out_kind: kOutBF16 / kOutF32 / kOutF16
     int ab_f16;
