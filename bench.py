@@ -57,12 +57,17 @@ def scan_pairs(B, T, causal):
 
 
 # DRAM bytes (read + write) per launch of each kernel kind, from the ncu
-# captures summarised in profiles/ (cold-cache replays).  Workloads captured
-# on a smaller case are scaled by the units processed (matrices, sequences),
-# which their traffic grows in proportion to.  Drop an entry whenever the
-# kernel changes after the capture.
+# captures summarised in profiles/ (cold-cache replays).  The MHA-layer
+# entries are captures of the bench workload itself.  The expert-batch
+# Newton-Schulz entry is an 8-matrix capture x 12: its working set already
+# exceeds L2 at 8 matrices, so traffic grows in proportion to the matrices.
+# Scans and projections of the MLA workloads are absent: their traffic does
+# not grow in proportion to the sequences (L2 reuse of K panels), so smaller
+# captures do not extrapolate.  Drop an entry whenever the kernel changes.
 TRAFFIC = {
-    ("c2", "scan"): 33611520,
+    ("c2", "scan"): 33612288,
+    ("c2", "gemm:ns"): 4279552 + 10752,
+    ("c4", "gemm:ns"): 12 * (3447001088 + 1815194624),
 }
 
 
