@@ -66,8 +66,6 @@ def scan_pairs(B, T, causal):
 # captures do not extrapolate.  Drop an entry whenever the kernel changes.
 TRAFFIC = {
     ("c2", "scan"): 33612288,
-    ("c2", "gemm:ns"): 4279552 + 10752,
-    ("c4", "gemm:ns"): 12 * (3447001088 + 1815194624),
 }
 
 

@@ -88,18 +88,23 @@ bool make_tmap_3d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t ou
     return r == CUDA_SUCCESS;
 }
 
+// Projection and plain GEMM launches use 256-row tiles computed by CTA pairs
+// (cta_group::2: each SM loads half of B).
+constexpr int kPairTileM = 2 * kBM;
+
 template <int MAXP>
 void finalize_gemm_params(GemmParamsT<MAXP>& P) {
     int begin = 0;
     if (P.bn <= 0) P.bn = kBN;
+    if (P.tile_m <= 0) P.tile_m = kBM;
     for (int i = 0; i < P.nprob; ++i) {
         GemmProblem& q = P.p[i];
-        q.tiles_m = (q.M + kBM - 1) / kBM;
+        q.tiles_m = (q.M + P.tile_m - 1) / P.tile_m;
         q.tiles_n = (q.N + P.bn - 1) / P.bn;
         if (q.sym) {
             // row block tm keeps the column tiles that reach the diagonal
             int t = 0;
-            for (int tm = 0; tm < q.tiles_m; ++tm) t += q.tiles_n - (kBM * tm) / P.bn;
+            for (int tm = 0; tm < q.tiles_m; ++tm) t += q.tiles_n - (P.tile_m * tm) / P.bn;
             q.tiles_per_batch = t;
         } else {
             q.tiles_per_batch = q.tiles_m * q.tiles_n;
@@ -342,6 +347,7 @@ mc_status mc_max_logits_mha(const void* x, const void* wq, const void* wk, mc_dt
         P.nprob = 2;
         if (!weight_problem(P.p[0], x, BT, D, D, wq, D, N, q, N, 0)) return MC_ERR_INVALID_ARG;
         if (!weight_problem(P.p[1], x, BT, D, D, wk, D, N, k, N, 0)) return MC_ERR_INVALID_ARG;
+        P.tile_m = kPairTileM;
         finalize_gemm_params(P);
         MC_CUDA(launch_gemm(P, stream, "gemm:proj"));
         ScanArgs a;
@@ -476,6 +482,7 @@ mc_status mc_max_logits_mla(const mc_mla_layer* L, const void* x, int B, int T, 
     P.p[1].rope_T = T;
     P.p[1].rope_period = kvw;
     P.p[1].rope_start = L->kv_lora;
+    P.tile_m = kPairTileM;
     finalize_gemm_params(P);
     MC_CUDA(launch_gemm(P, stream, "gemm:proj"));
     // phase 2: [q^C | q^R] = c_Q W_qb (RoPE on q^R) ; k^C = c_KV W_kb, on
@@ -493,6 +500,7 @@ mc_status mc_max_logits_mla(const mc_mla_layer* L, const void* x, int B, int T, 
     P.p[0].rope_start = L->nope;
     if (!weight_problem(P.p[1], w.ckv, BT, L->kv_lora, kvw, w.wkb, L->kv_lora, Nk, w.kc, Nk, 1))
         return MC_ERR_INVALID_ARG;
+    P.tile_m = kPairTileM;
     finalize_gemm_params(P);
     MC_CUDA(launch_gemm(P, stream, "gemm:proj"));
     // scan: per head 3 K blocks (q^C.k^C x2, q^R.k^R x1)
@@ -751,7 +759,8 @@ mc_status run_norm(const NsPlan& P, float eps, cudaStream_t stream) {
 // them (exactly symmetric A, B); otherwise every tile is computed, which
 // costs no time when the full tiling still fits the same number of waves.
 bool ns_problem(GemmProblem& q, const NsPlan& P, const NsGroup& gr, int kind, int it, float a, float b,
-                float c, int bn, int sym) {
+                float c, int bn, int sym, int tile_m) {
+    const uint32_t brows = tile_m == kBM ? bn : bn / 2;  // K-major B rows loaded per CTA
     memset(&q, 0, sizeof(q));
     const int xin = it & 1, xout = (it + 1) & 1;
     const uint64_t cnt = gr.idx.size(), mp = gr.m_pad, np = gr.n_pad;
@@ -766,7 +775,7 @@ bool ns_problem(GemmProblem& q, const NsPlan& P, const NsGroup& gr, int kind, in
     }
     if (kind == 0) {
         if (!make_tmap_3d(&q.tmA, gr.X[xin], np, mp, cnt, np, mp * np, kBK, kBM, 0)) return false;
-        if (!make_tmap_3d(&q.tmB, gr.X[xin], np, mp, cnt, np, mp * np, kBK, bn, 0)) return false;
+        if (!make_tmap_3d(&q.tmB, gr.X[xin], np, mp, cnt, np, mp * np, kBK, brows, 0)) return false;
         q.M = q.N = (int)mp;
         q.K = (int)np;
         q.sym = sym;
@@ -777,7 +786,7 @@ bool ns_problem(GemmProblem& q, const NsPlan& P, const NsGroup& gr, int kind, in
         q.scale = it == 0 ? P.s2 + gr.zbase : nullptr;
     } else if (kind == 1) {
         if (!make_tmap_3d(&q.tmA, gr.A, mp, mp, cnt, mp, mp * mp, kBK, kBM, 0)) return false;
-        if (!make_tmap_3d(&q.tmB, gr.A, mp, mp, cnt, mp, mp * mp, kBK, bn, 0)) return false;
+        if (!make_tmap_3d(&q.tmB, gr.A, mp, mp, cnt, mp, mp * mp, kBK, brows, 0)) return false;
         q.M = q.N = q.K = (int)mp;
         q.sym = sym;
         q.out = gr.Bm;
@@ -817,25 +826,29 @@ mc_status run_ns_iterations(const NsPlan& P, int steps, float a, float b, float 
     for (int g0 = 0; g0 < ngroups; g0 += 4) {
         const int g1 = std::min(ngroups, g0 + 4);
         const int per_launch = std::min(kMaxPhases / 3, kMaxProblemsMulti / (3 * (g1 - g0)));
-        // 128-column tiles (6-stage ring) when 256-column tiles of the apply
-        // phase would leave SMs idle
+        // Large batches: 256 x 256 tiles computed by CTA pairs (m_pad is a
+        // multiple of 256).  Batches whose apply phase has fewer such tiles
+        // than SM pairs: 128 x 128 tiles on single CTAs, where the pairs'
+        // cross-SM hand-offs cost more than the halved B loads save.
         long long apply_tiles = 0;
         for (int g = g0; g < g1; ++g) {
             const NsGroup& gr = P.groups[g];
-            apply_tiles += (long long)gr.idx.size() * (gr.m_pad / kBM) * ((gr.n_pad + kBN - 1) / kBN);
+            apply_tiles += (long long)gr.idx.size() * (gr.m_pad / kPairTileM) * ((gr.n_pad + kBN - 1) / kBN);
         }
-        const int bn = apply_tiles < num_sms() ? 128 : kBN;
+        const bool small = apply_tiles < num_sms() / 2;
+        const int bn = small ? 128 : kBN;
+        const int tile_m = small ? kBM : kPairTileM;
+        const long long nsm = small ? num_sms() : num_sms() / 2;  // scheduling units
         // full Gram / poly tilings when they take no more waves than the symmetric ones
         long long sym_tiles = 0, full_tiles = 0;
         for (int g = g0; g < g1; ++g) {
             const NsGroup& gr = P.groups[g];
-            const long long tm = gr.m_pad / kBM, tn = (gr.m_pad + bn - 1) / bn;
+            const long long tm = gr.m_pad / tile_m, tn = (gr.m_pad + bn - 1) / bn;
             long long t = 0;
-            for (long long i = 0; i < tm; ++i) t += tn - (kBM * i) / bn;
+            for (long long i = 0; i < tm; ++i) t += tn - (tile_m * i) / bn;
             sym_tiles += (long long)gr.idx.size() * t;
             full_tiles += (long long)gr.idx.size() * tm * tn;
         }
-        const long long nsm = num_sms();
         const int sym = (full_tiles + nsm - 1) / nsm > (sym_tiles + nsm - 1) / nsm ? 1 : 0;
         for (int it0 = 0; it0 < steps; it0 += per_launch) {
             const int nit = std::min(per_launch, steps - it0);
@@ -843,11 +856,12 @@ mc_status run_ns_iterations(const NsPlan& P, int steps, float a, float b, float 
             std::lock_guard<std::mutex> lk(g_launch_mu);
             memset(&G, 0, sizeof(G));
             G.bn = bn;
+            G.tile_m = tile_m;
             for (int it = it0; it < it0 + nit; ++it)
                 for (int kind = 0; kind < 3; ++kind) {
                     G.phase_prob[G.nphase++] = G.nprob;
                     for (int g = g0; g < g1; ++g)
-                        if (!ns_problem(G.p[G.nprob++], P, P.groups[g], kind, it, a, b, c, bn, sym))
+                        if (!ns_problem(G.p[G.nprob++], P, P.groups[g], kind, it, a, b, c, bn, sym, tile_m))
                             return MC_ERR_CUDA;
                 }
             G.phase_prob[G.nphase] = G.nprob;
@@ -940,11 +954,14 @@ mc_status mc_gemm_bf16(const void* a, const void* b, void* c, mc_dtype c_type, i
     GemmParams P;
     memset(&P, 0, sizeof(P));
     P.nprob = 1;
+    P.tile_m = kPairTileM;
     GemmProblem& q = P.p[0];
     const uint64_t m = M, n = N, k = K, z = batch;
     if (!make_tmap_3d(&q.tmA, a, k, m, z, k, m * k, kBK, kBM, 0)) return MC_ERR_INVALID_ARG;
     if (b_kmajor) {
-        if (!make_tmap_3d(&q.tmB, b, k, n, z, k, n * k, kBK, kBN, 0)) return MC_ERR_INVALID_ARG;
+        // a CTA of a pair loads half of the B tile's rows
+        const uint32_t brows = P.tile_m == kBM ? kBN : kBN / 2;
+        if (!make_tmap_3d(&q.tmB, b, k, n, z, k, n * k, kBK, brows, 0)) return MC_ERR_INVALID_ARG;
     } else {
         if (!make_tmap_3d(&q.tmB, b, n, k, z, n, k * n, 64, kBK, 0)) return MC_ERR_INVALID_ARG;
         q.b_mn = 1;

@@ -33,9 +33,9 @@ static_assert(kEpiWarpBytes >= 32 * kStageLd * 2 && kEpiWarpBytes % 1024 == 0, "
 // 128-byte rows (segment v stored at v ^ (r mod 8): conflict-free and the
 // layout a SWIZZLE_128B tensor map reads).
 MC_D int stage_off(bool swz, int r, int v) { return swz ? r * 64 + ((v ^ (r & 7)) << 3) : r * kStageLd + (v << 3); }
-// Tile / pipeline shapes: BN = 256 with 4 stages of 48 KB (large problems),
-// BN = 128 with 6 stages of 32 KB (small Newton-Schulz batches: twice the
-// tiles per phase, so more SMs share each phase, and more stages in flight).
+// Tile / pipeline shapes (see the launchers at the end): CTA pairs on
+// 256 x 256 tiles, each SM holding 128 rows of A and 128 of B per 32 KB
+// stage; single CTAs on 128 x 128 tiles for small Newton-Schulz batches.
 // Shared-memory copies of the current and the next phase's problems: the
 // roles read the problem fields from here instead of the (large, dynamically
 // indexed) kernel parameters, whose constant-cache misses would otherwise sit
@@ -43,14 +43,17 @@ MC_D int stage_off(bool swz, int r, int v) { return swz ? r * 64 + ((v ^ (r & 7)
 // parameters.
 constexpr int kTailBytes = 384;
 constexpr int kProbStageBytes = 2 * kPhaseProbs * (int)sizeof(GemmProblem);
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool PAIR = false>
 struct TileCfg {
-    static constexpr int kBStage = BN * kBK * 2;
+    // a pair computes a 256 x BN tile: each CTA holds 128 rows of A and BN / 2
+    // rows (K-major) or columns (MN-major) of B; the MMA reads both halves
+    static constexpr int kTileM = PAIR ? 2 * kBM : kBM;
+    static constexpr int kBRows = PAIR ? BN / 2 : BN;
+    static constexpr int kBStage = kBRows * kBK * 2;
     static constexpr int kSmem = STAGES * (kAStageBytes + kBStage) + 4 * kEpiWarpBytes + 1024 + kTailBytes +
                                  64 + kProbStageBytes;
     static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
 };
-
 template <int STAGES>
 struct GemmSmemTail {
     uint64_t full[STAGES];
@@ -64,7 +67,7 @@ struct GemmSmemTail {
 
 // Tile t of a phase -> (problem index within the phase, batch, row block,
 // column block); sp holds the phase's np problems.
-template <int BN>
+template <int BN, int TM>
 MC_D void decode_tile(const GemmProblem* sp, int np, int t, int& pi, int& z, int& tm, int& tn) {
     pi = 0;
     while (pi + 1 < np && t >= sp[pi + 1].tile_begin) ++pi;
@@ -76,10 +79,10 @@ MC_D void decode_tile(const GemmProblem* sp, int np, int t, int& pi, int& z, int
         tm = r / q.tiles_n;
         tn = r - tm * q.tiles_n;
     } else {
-        // row block tm holds the tiles tn >= 128 tm / BN (those touching c >= r)
+        // row block tm holds the tiles tn >= TM tm / BN (those touching c >= r)
         tm = 0;
         while (true) {
-            const int first = (kBM * tm) / BN;
+            const int first = (TM * tm) / BN;
             int cnt = q.tiles_n - first;
             if (r < cnt) {
                 tn = first + r;
@@ -424,9 +427,10 @@ MC_D void norm_prephase(const GemmParamsT<MAXP>& P, double* red) {
     }
 }
 
-template <int MAXP, int BN, int STAGES>
+template <int MAXP, int BN, int STAGES, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParamsT<MAXP> P) {
-    using Cfg = TileCfg<BN, STAGES>;
+    using Cfg = TileCfg<BN, STAGES, PAIR>;
+    constexpr int TM = Cfg::kTileM;
     constexpr int kBStageBytes = Cfg::kBStage;
     constexpr int kGemmStages = STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -442,6 +446,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // pair mode: cluster of two CTAs; rank 0 issues the MMAs of the pair
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0;
+    const bool leader = rank == 0;
+    const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int nunits = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kGemmStages; ++s) {
@@ -450,7 +459,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tail->tfull[a], 1);
-            mbar_init(&tail->tempty[a], 4);
+            mbar_init(&tail->tempty[a], PAIR ? 8 : 4);  // pair: both CTAs' epilogue warps
         }
         mbar_init(&tail->drain, 1);
         tail->abort_flag = 0;
@@ -464,12 +473,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         }
     }
     if (warp == 1) {
-        tmem_alloc(&tail->tmem_base, Cfg::kTmemCols);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(&tail->tmem_base, Cfg::kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(&tail->tmem_base, Cfg::kTmemCols);
+            tmem_relinquish();
+        }
     }
     if (warp >= 2) stage_phase(P, 0, sProb, threadIdx.x - 64, blockDim.x - 64);
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();  // both CTAs' barriers and TMEM exist before any remote use
     tc_fence_after();
     const uint32_t tmem_base = tail->tmem_base;
     pdl_wait();  // the previous kernel's outputs are our inputs
@@ -496,9 +511,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         if (warp == 0) {
             // ---------------- TMA producer ----------------
             if (lane == 0 && ok) {
-                for (int t = t_begin + blockIdx.x; t < t_end && ok; t += gridDim.x) {
+                for (int t = t_begin + unit; t < t_end && ok; t += nunits) {
                     int pi, z, tm, tn;
-                    decode_tile<BN>(sp, np, t, pi, z, tm, tn);
+                    decode_tile<BN, TM>(sp, np, t, pi, z, tm, tn);
                     const GemmProblem& q = sp[pi];
                     const CUtensorMap* tmA = &P.p[pb + pi].tmA;
                     const CUtensorMap* tmB = &P.p[pb + pi].tmB;
@@ -508,16 +523,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(&tail->full[stage], kAStageBytes + kBStageBytes);
-                        tma_load_3d(sA + stage * kAStageBytes, tmA, &tail->full[stage], kb * kBK, tm * kBM, z);
                         uint8_t* b = sB + stage * kBStageBytes;
-                        if (!q.b_mn) {
-                            tma_load_3d(b, tmB, &tail->full[stage], kb * kBK, tn * BN, z);
-                        } else {
+                        if constexpr (PAIR) {
+                            // both halves complete on the leader's full barrier, which expects both
+                            if (leader) mbar_arrive_expect_tx(&tail->full[stage], 2 * (kAStageBytes + kBStageBytes));
+                            const uint32_t fb = mapa_shared(smem_u32(&tail->full[stage]), 0);
+                            tma_load_3d_pair(sA + stage * kAStageBytes, tmA, fb, kb * kBK, tm * TM + rank * kBM, z);
+                            const int b0 = tn * BN + (int)rank * Cfg::kBRows;
+                            if (!q.b_mn) {
+                                tma_load_3d_pair(b, tmB, fb, kb * kBK, b0, z);
+                            } else {
 #pragma unroll
-                            for (int j = 0; j < BN / 64; ++j)
-                                tma_load_3d(b + j * (kBK * 128), tmB, &tail->full[stage], tn * BN + j * 64,
-                                            kb * kBK, z);
+                                for (int j = 0; j < Cfg::kBRows / 64; ++j)
+                                    tma_load_3d_pair(b + j * (kBK * 128), tmB, fb, b0 + j * 64, kb * kBK, z);
+                            }
+                        } else {
+                            mbar_arrive_expect_tx(&tail->full[stage], kAStageBytes + kBStageBytes);
+                            tma_load_3d(sA + stage * kAStageBytes, tmA, &tail->full[stage], kb * kBK, tm * kBM, z);
+                            if (!q.b_mn) {
+                                tma_load_3d(b, tmB, &tail->full[stage], kb * kBK, tn * BN, z);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < BN / 64; ++j)
+                                    tma_load_3d(b + j * (kBK * 128), tmB, &tail->full[stage], tn * BN + j * 64,
+                                                kb * kBK, z);
+                            }
                         }
                         ++issued[stage];
                         if (++stage == kGemmStages) {
@@ -528,13 +558,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 }
             }
         } else if (warp == 1) {
-            // ---------------- MMA issuer ----------------
-            for (int t = t_begin + blockIdx.x; t < t_end && ok; t += gridDim.x) {
+            // ---------------- MMA issuer (the leader of a pair) ----------------
+            for (int t = t_begin + unit; t < t_end && ok && leader; t += nunits) {
                 int pi, z, tm, tn;
-                decode_tile<BN>(sp, np, t, pi, z, tm, tn);
+                decode_tile<BN, TM>(sp, np, t, pi, z, tm, tn);
                 const GemmProblem& q = sp[pi];
                 const int nk = (q.K + kBK - 1) / kBK;
-                const uint32_t idesc = idesc_f16kind(kBM, BN, q.b_mn, q.ab_f16);
+                const uint32_t idesc = idesc_f16kind(TM, BN, q.b_mn, q.ab_f16);
                 if (!mbar_wait(&tail->tempty[acc], aphase ^ 1, abort_flag, P.status)) {
                     ok = false;
                     break;
@@ -555,9 +585,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                             uint64_t ad = sw128_desc(a0 + k * 32, 16, 1024);
                             uint64_t bd = q.b_mn ? sw128_desc(b0 + k * 2048, kBK * 128, 1024)
                                                  : sw128_desc(b0 + k * 32, 16, 1024);
-                            umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0);
+                            if constexpr (PAIR)
+                                umma_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
+                            else
+                                umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0);
                         }
-                        umma_commit(&tail->empty[stage]);
+                        if constexpr (PAIR)
+                            umma_commit_pair_both(&tail->empty[stage]);  // both producers may refill
+                        else
+                            umma_commit(&tail->empty[stage]);
                     }
                     __syncwarp();
                     if (++stage == kGemmStages) {
@@ -566,7 +602,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                     }
                 }
                 if (!ok) break;
-                if (lane == 0) umma_commit(&tail->tfull[acc]);
+                if (lane == 0) {
+                    if constexpr (PAIR)
+                        umma_commit_pair_both(&tail->tfull[acc]);  // both epilogues
+                    else
+                        umma_commit(&tail->tfull[acc]);
+                }
                 __syncwarp();
                 if (++acc == 2) {
                     acc = 0;
@@ -577,19 +618,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             // ---------------- epilogue (warps 2..5) ----------------
             const int quarter = warp & 3;  // TMEM lanes this warp may access
             uint16_t* S = sEpi + (warp - 2) * (kEpiWarpBytes / 2);
-            for (int t = t_begin + blockIdx.x; t < t_end && ok; t += gridDim.x) {
+            for (int t = t_begin + unit; t < t_end && ok; t += nunits) {
                 int pi, z, tm, tn;
-                decode_tile<BN>(sp, np, t, pi, z, tm, tn);
+                decode_tile<BN, TM>(sp, np, t, pi, z, tm, tn);
                 const GemmProblem& q = sp[pi];
                 const bool staged = q.vec_ok && q.out_kind != kOutF32;
+                const int row0 = tm * TM + (int)rank * kBM + quarter * 32;
                 uint4 u[8] = {};
-                if (staged && q.aux) aux_load(q, z, tm * kBM + quarter * 32, tn * BN, u);
+                if (staged && q.aux) aux_load(q, z, row0, tn * BN, u);
                 if (!mbar_wait(&tail->tfull[acc], aphase, abort_flag, P.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const int row0 = tm * kBM + quarter * 32;
                 const int r = row0 + lane;
                 const float sc = q.scale ? q.scale[z] : 1.0f;
 #pragma unroll 1
@@ -608,7 +649,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&tail->tempty[acc]);
+                if (lane == 0) {
+                    if (PAIR && !leader)
+                        mbar_arrive_cluster(mapa_shared(smem_u32(&tail->tempty[acc]), 0));
+                    else
+                        mbar_arrive(&tail->tempty[acc]);
+                }
                 if (++acc == 2) {
                     acc = 0;
                     aphase ^= 1;
@@ -621,14 +667,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         if (ph + 1 < P.nphase) grid_sync(P, nsync++, abort_flag, ph + 1, sProb + ((ph + 1) & 1) * kPhaseProbs);
     }
 
-    if (warp == 0 && lane == 0) {
-        // wait for this thread's copies still in flight before exit
+    if (warp == 0 && lane == 0 && leader) {
+        // wait for the copies still in flight before exit (a pair's copies all
+        // complete on the leader's barriers; the final cluster barrier keeps
+        // the other CTA resident until then)
         volatile int never = 0;
         for (int s = 0; s < kGemmStages; ++s)
             if (issued[s]) mbar_wait(&tail->full[s], (issued[s] - 1) & 1, &never, P.status);
-    } else if (warp == 1) {
+    } else if (warp == 1 && leader) {
         // drain: every MMA this thread issued has completed before teardown
-        if (lane == 0) umma_commit(&tail->drain);
+        if (lane == 0) {
+            if constexpr (PAIR)
+                umma_commit_pair(&tail->drain);
+            else
+                umma_commit(&tail->drain);
+        }
         __syncwarp();
         volatile int never = 0;
         mbar_wait(&tail->drain, 0, &never, P.status);
@@ -637,18 +690,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     pdl_trigger();
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();  // the leader's MMAs and remote arrivals are done
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    if (warp == 1) {
+        if constexpr (PAIR)
+            tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+        else
+            tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    }
 }
 
-template <int MAXP, int BN, int STAGES>
+template <int MAXP, int BN, int STAGES, bool PAIR>
 static cudaError_t set_smem_attr() {
     static bool attr_set[64] = {false};
     int dev = current_device();
     if (dev < 0) return cudaErrorInvalidDevice;
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<MAXP, BN, STAGES>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, TileCfg<BN, STAGES>::kSmem);
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<MAXP, BN, STAGES, PAIR>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             TileCfg<BN, STAGES, PAIR>::kSmem);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
@@ -667,45 +727,61 @@ static bool phases_fit(const GemmParamsT<MAXP>& P) {
     return P.phase_prob[P.nphase] == P.nprob;
 }
 
-cudaError_t launch_gemm(const GemmParams& P, cudaStream_t stream, const char* label) {
-    if (P.total_tiles <= 0) return cudaSuccess;
-    if (P.bn != kBN || !phases_fit(P)) return cudaErrorInvalidValue;
-    cudaError_t e = set_smem_attr<kMaxProblems, kBN, kGemmStages>();
+// One persistent CTA (pair: one cluster of two CTAs) per SM (pair of SMs),
+// no more than there are tiles; cooperative launches keep every CTA resident
+// for the grid barriers between phases.
+template <int MAXP, int BN, int STAGES, bool PAIR>
+static cudaError_t launch_cfg(const GemmParamsT<MAXP>& P, bool coop, cudaStream_t stream, const char* label) {
+    using Cfg = TileCfg<BN, STAGES, PAIR>;
+    if (P.tile_m != Cfg::kTileM || P.bn != BN) return cudaErrorInvalidValue;
+    cudaError_t e = set_smem_attr<MAXP, BN, STAGES, PAIR>();
     if (e != cudaSuccess) return e;
-    int grid = num_sms();
-    if (grid > P.total_tiles) grid = P.total_tiles;
+    int units = PAIR ? num_sms() / 2 : num_sms();
+    if (!coop && units > P.total_tiles) units = P.total_tiles;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(PAIR ? 2 * units : units);
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = Cfg::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (coop) {
+        attr[na].id = cudaLaunchAttributeCooperative;
+        attr[na].val.cooperative = 1;
+        ++na;
+    } else {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    if (PAIR) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 2;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
     TraceScope ts(label, stream);
-    return launch_pdl(gemm_kernel<kMaxProblems, kBN, kGemmStages>, dim3(grid), dim3(kGemmThreads),
-                      TileCfg<kBN, kGemmStages>::kSmem, stream, P);
+    e = cudaLaunchKernelEx(&cfg, gemm_kernel<MAXP, BN, STAGES, PAIR>, P);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-// All phases in one cooperative launch: one CTA per SM, every CTA resident,
-// grid barriers between phases.
-template <int BN, int STAGES>
-static cudaError_t launch_multi_cfg(const GemmParamsMulti& P, cudaStream_t stream, const char* label) {
-    cudaError_t e = set_smem_attr<kMaxProblemsMulti, BN, STAGES>();
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(num_sms());
-    cfg.blockDim = dim3(kGemmThreads);
-    cfg.dynamicSmemBytes = TileCfg<BN, STAGES>::kSmem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    TraceScope ts(label, stream);
-    e = cudaLaunchKernelEx(&cfg, gemm_kernel<kMaxProblemsMulti, BN, STAGES>, P);
-    return e != cudaSuccess ? e : cudaGetLastError();
+// Configurations: 256 x 256 tiles on CTA pairs with 6 stages of 32 KB per
+// SM (projections, plain GEMMs, large Newton-Schulz batches); 128 x 128
+// tiles on single CTAs with 6 stages of 32 KB (small Newton-Schulz batches).
+cudaError_t launch_gemm(const GemmParams& P, cudaStream_t stream, const char* label) {
+    if (P.total_tiles <= 0) return cudaSuccess;
+    if (!phases_fit(P)) return cudaErrorInvalidValue;
+    return launch_cfg<kMaxProblems, kBN, 6, true>(P, false, stream, label);
 }
 
 cudaError_t launch_gemm_multi(const GemmParamsMulti& P, cudaStream_t stream, const char* label) {
     if (P.total_tiles <= 0) return cudaSuccess;
     if (!phases_fit(P)) return cudaErrorInvalidValue;
-    if (P.bn == 128) return launch_multi_cfg<128, 6>(P, stream, label);
-    if (P.bn == kBN) return launch_multi_cfg<kBN, kGemmStages>(P, stream, label);
-    return cudaErrorInvalidValue;
+    if (P.tile_m == 2 * kBM) return launch_cfg<kMaxProblemsMulti, kBN, 6, true>(P, true, stream, label);
+    return launch_cfg<kMaxProblemsMulti, 128, 6, false>(P, true, stream, label);
 }
 
 }  // namespace mc

@@ -19,7 +19,6 @@ namespace mc {
 constexpr int kBM = 128;  // UMMA M (TMEM lanes)
 constexpr int kBN = 256;  // UMMA N (TMEM columns per accumulator)
 constexpr int kBK = 64;   // K per smem stage: one 128-byte swizzle row of bf16
-constexpr int kGemmStages = 4;
 constexpr int kMaxProblems = 4;        // problems of a single-phase launch
 constexpr int kMaxProblemsMulti = 48;  // problems of a multi-phase launch (kernel parameters < 32 KB)
 constexpr int kMaxPhases = 16;
@@ -69,7 +68,8 @@ template <int MAXP>
 struct GemmParamsT {
     GemmProblem p[MAXP];
     int nprob, total_tiles;
-    int bn;  // output tile width of the launch: 256 (default when 0) or 64
+    int bn;      // output tile width of the launch: 256 (default when 0) or 128
+    int tile_m;  // output tile height: 128 (one CTA, default when 0) or 256 (a CTA pair)
     int nphase;
     int phase_prob[kMaxPhases + 1];
     unsigned* grid_bar;
