@@ -39,6 +39,7 @@ struct ScanParams {
     int B, T, H, causal;
     int q_head_stride, k_head_stride, nkb_main, nkb_rope, kr_col;
     int n_it, total_items;
+    int band;  // (sequence, head) pairs per band of the item order
     unsigned* keys;
     unsigned* done;  // zeroed counter of finished CTAs
     float sqrt_d;
@@ -76,15 +77,30 @@ MC_D void finalize_head(const unsigned* keys, int B, int H, int h, float sqrt_d,
     s_max[h] = s;
 }
 
+// Item order: bands of P.band (sequence, head) pairs; within a band the
+// query tiles go heaviest causal tile first, pairs minor.  The items running
+// at one time then share the K panels of a few pairs (which stay in L2)
+// instead of touching one panel per CTA.
 MC_D void decode_item(const ScanParams& P, int i, int& b, int& h, int& it, int& njt) {
     const int BH = P.B * P.H;
-    int grp = i / BH;
-    int bh = i - grp * BH;
+    const int per_band = P.band * P.n_it;
+    const int band = i / per_band;
+    const int w = i - band * per_band;
+    const int pairs = min(P.band, BH - band * P.band);  // the last band may be short
+    const int grp = w / pairs;
+    const int bh = band * P.band + (w - grp * pairs);
     it = P.causal ? (P.n_it - 1 - grp) : grp;
     b = bh / P.H;
     h = bh - b * P.H;
     int row_end = min(P.T, (it + 1) * kBM);  // exclusive
     njt = P.causal ? ((row_end - 1) / kBN + 1) : ((P.T + kBN - 1) / kBN);
+}
+
+// The i-th item of round r for this CTA: rounds are dealt in snake order
+// (forward, then backward), which pairs heavy with light causal items.
+MC_D int item_of_round(int r) {
+    const int c = (r & 1) ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+    return r * (int)gridDim.x + c;
 }
 
 __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(const __grid_constant__ ScanParams P) {
@@ -137,7 +153,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(const __grid_cons
             uint32_t issued[kScanStages] = {0, 0, 0, 0};
             uint32_t n = 0;  // items started by this CTA: Q buffer n & 1
             bool ok = true;
-            for (int i = blockIdx.x; i < P.total_items && ok; i += gridDim.x, ++n) {
+            for (int r = 0, i = item_of_round(0); i < P.total_items && ok; i = item_of_round(++r), ++n) {
                 int b, h, it, njt;
                 decode_item(P, i, b, h, it, njt);
                 const int qb = n & 1;
@@ -180,7 +196,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(const __grid_cons
         uint32_t n = 0;
         bool ok = true;
         const uint32_t idesc = idesc_f16kind(kBM, kBN, 0, 1);  // fp16 Q and K
-        for (int i = blockIdx.x; i < P.total_items && ok; i += gridDim.x, ++n) {
+        for (int r = 0, i = item_of_round(0); i < P.total_items && ok; i = item_of_round(++r), ++n) {
             int b, h, it, njt;
             decode_item(P, i, b, h, it, njt);
             const int qb = n & 1;
@@ -236,7 +252,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(const __grid_cons
         int acc = 0;
         uint32_t aphase = 0;
         bool ok = true;
-        for (int i = blockIdx.x; i < P.total_items && ok; i += gridDim.x) {
+        for (int r = 0, i = item_of_round(0); i < P.total_items && ok; i = item_of_round(++r)) {
             int b, h, it, njt;
             decode_item(P, i, b, h, it, njt);
             const int row = it * kBM + quarter * 32 + lane;
@@ -361,6 +377,8 @@ cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream) {
     }
     int grid = num_sms();
     if (grid > P.total_items) grid = P.total_items;
+    // about two rounds of items per band
+    P.band = std::max(1, std::min(a.B * a.H, (2 * grid + P.n_it - 1) / P.n_it));
     TraceScope ts("scan", stream);
     return launch_pdl(scan_kernel, dim3(grid), dim3(kScanThreads), kScanSmem, stream, P);
 }
