@@ -210,6 +210,8 @@ static bool weight_problem(GemmProblem& q, const void* a, int64_t a_rows, int64_
     q.alpha = 1.f;
     q.beta = 0.f;
     q.vec_ok = (out_ld % 8 == 0) && aligned16(out);
+    // fp16 output chunks leave through one TMA tensor store each
+    q.bulk_st = q.vec_ok && make_tmap_3d(&q.tmC, out, N, a_rows, 1, out_ld, 0, 64, 32, 1);
     return true;
 }
 
@@ -976,6 +978,8 @@ mc_status mc_gemm_bf16(const void* a, const void* b, void* c, mc_dtype c_type, i
     q.out_bstride = (long long)M * N;
     q.alpha = 1.f;
     q.vec_ok = c_type == MC_F32 ? (N % 4 == 0) : (N % 8 == 0);
+    if (c_type == MC_BF16 && q.vec_ok)
+        q.bulk_st = make_tmap_3d(&q.tmC, c, n, m, z, n, m * n, 64, 32, 0);
     finalize_gemm_params(P);
     MC_CUDA(launch_gemm(P, (cudaStream_t)stream, "gemm"));
     return MC_OK;
