@@ -116,9 +116,17 @@ MC_D void grid_sync(const GemmParamsT<MAXP>& P, int seq, volatile int* abort_fla
     // the other threads stage the next phase's problems while thread 0 waits
     if (next_ph >= 0 && threadIdx.x >= 32) stage_phase(P, next_ph, next_dst, threadIdx.x - 32, blockDim.x - 32);
     if (threadIdx.x == 0) {
-        __threadfence();
+        // release the CTA's phase writes (ordered before by the CTA barrier)
+        // with the arrival itself; no returned value to wait for
         asm volatile("fence.proxy.async.global;" ::: "memory");
-        atomicAdd(P.grid_bar, 1u);
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(P.grid_bar) : "memory");
+        // the next phase's tensor maps into the TMA descriptor cache meanwhile
+        if (next_ph >= 0)
+            for (int i = P.phase_prob[next_ph]; i < P.phase_prob[next_ph + 1]; ++i) {
+                tma_prefetch_desc(&P.p[i].tmA);
+                tma_prefetch_desc(&P.p[i].tmB);
+                if (P.p[i].bulk_st) tma_prefetch_desc(&P.p[i].tmC);
+            }
         const unsigned target = (unsigned)(seq + 1) * gridDim.x;
         uint64_t t0 = 0;
         while (true) {

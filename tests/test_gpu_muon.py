@@ -100,3 +100,20 @@ def test_lr_zero_leaves_weights_bit_unchanged():
                      [torch.zeros(128, 256, device=dev())], lr=0.0)
     torch.cuda.synchronize()
     assert torch.equal(wd_.cpu(), w)
+
+
+def test_newton_schulz_pair_tiles_symmetric():
+    """A batch large enough for 256 x 256 CTA-pair tiles whose Gram and A.A
+    use the symmetric upper-tile schedule (192 symmetric against 280 full
+    Gram tiles), in two shape groups: 16 wide 512 x 1024 matrices and 24 tall
+    1024 x 768 ones (iterated transposed)."""
+    lib()
+    from muonclip_mc_max_gb300 import api
+    shapes = [(512, 1024)] * 16 + [(1024, 768)] * 24
+    mats = [mc_inputs.matrix(r, c, seed=700 + i) for i, (r, c) in enumerate(shapes)]
+    outs = api.mc_newton_schulz([m.to(dev()) for m in mats])
+    torch.cuda.synchronize()
+    for i in (0, 15, 16, 39):
+        assert rel_fro(outs[i].cpu().numpy(), oracle.newton_schulz_np(mats[i])) < NS_RTOL, i
+    for o in outs:
+        assert bool(torch.isfinite(o).all())
