@@ -57,16 +57,17 @@ def scan_pairs(B, T, causal):
 
 
 # DRAM bytes (read + write) per launch of each kernel kind, from the ncu
-# captures summarised in profiles/ (cold-cache replays).  The MHA-layer
-# entries are captures of the bench workload itself.  The expert-batch
-# Newton-Schulz entry is an 8-matrix capture x 12: its working set already
-# exceeds L2 at 8 matrices, so traffic grows in proportion to the matrices.
-# Scans and projections of the MLA workloads are absent: their traffic does
-# not grow in proportion to the sequences (L2 reuse of K panels), so smaller
-# captures do not extrapolate.  Drop an entry whenever the kernel changes.
+# captures summarised in profiles/ (cold-cache replays), all taken on the
+# bench workloads themselves (1-pass metric sets on the large ones).  The
+# expert-batch Newton-Schulz launch (cooperative, on CTA pairs) cannot be
+# captured by ncu and has no entry.  Drop an entry whenever the kernel changes.
 TRAFFIC = {
     ("c2", "scan"): 33612544,
-    ("c2", "gemm:ns"): 4291584 + 1280,
+    ("c2", "gemm:ns"): 4280576 + 4864,
+    # the two projection launches of the K2-shaped layer, averaged per launch
+    ("c3", "gemm:proj"): (2354066688 + 270765824 + 1171430656 + 2626077184) // 2,
+    ("c3", "scan"): 2933748736 + 143360,
+    ("c5", "scan"): 1450577664 + 3536896,
 }
 
 
