@@ -64,8 +64,6 @@ def scan_pairs(B, T, causal):
 TRAFFIC = {
     ("c2", "scan"): 33612544,
     ("c2", "gemm:ns"): 4280576 + 4864,
-    # the two projection launches of the K2-shaped layer, averaged per launch
-    ("c3", "gemm:proj"): (2354066688 + 270765824 + 1171430656 + 2626077184) // 2,
     ("c3", "scan"): 2933748736 + 143360,
     ("c5", "scan"): 1450577664 + 3536896,
 }

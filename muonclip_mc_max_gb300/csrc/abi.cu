@@ -113,6 +113,20 @@ void finalize_gemm_params(GemmParamsT<MAXP>& P) {
         begin += q.tiles_per_batch * q.batch;
     }
     P.total_tiles = begin;
+    // shared A (one phase, same rows, batch 1, not symmetric): every row
+    // block's column tiles of all problems run together, so A is read once
+    bool shared = P.a_shared && P.nphase <= 1 && P.nprob > 1;
+    for (int i = 0; shared && i < P.nprob; ++i)
+        shared = P.p[i].M == P.p[0].M && P.p[i].batch == 1 && !P.p[i].sym;
+    int tn = 0;
+    for (int i = 0; i < P.nprob; ++i) {
+        GemmProblem& q = P.p[i];
+        q.a_shared = shared ? 1 : 0;
+        q.tn_off = shared ? tn : 0;
+        tn += q.tiles_n;
+        if (shared) q.tile_begin = 0;
+    }
+    P.a_shared = shared ? 1 : 0;
     P.status = device_status_ptr();
     if (P.nphase <= 0) {
         P.nphase = 1;
@@ -350,6 +364,7 @@ mc_status mc_max_logits_mha(const void* x, const void* wq, const void* wk, mc_dt
         if (!weight_problem(P.p[0], x, BT, D, D, wq, D, N, q, N, 0)) return MC_ERR_INVALID_ARG;
         if (!weight_problem(P.p[1], x, BT, D, D, wk, D, N, k, N, 0)) return MC_ERR_INVALID_ARG;
         P.tile_m = kPairTileM;
+        P.a_shared = 1;
         finalize_gemm_params(P);
         MC_CUDA(launch_gemm(P, stream, "gemm:proj"));
         ScanArgs a;
@@ -485,6 +500,7 @@ mc_status mc_max_logits_mla(const mc_mla_layer* L, const void* x, int B, int T, 
     P.p[1].rope_period = kvw;
     P.p[1].rope_start = L->kv_lora;
     P.tile_m = kPairTileM;
+    P.a_shared = 1;
     finalize_gemm_params(P);
     MC_CUDA(launch_gemm(P, stream, "gemm:proj"));
     // phase 2: [q^C | q^R] = c_Q W_qb (RoPE on q^R) ; k^C = c_KV W_kb, on

@@ -69,6 +69,17 @@ struct GemmSmemTail {
 // column block); sp holds the phase's np problems.
 template <int BN, int TM>
 MC_D void decode_tile(const GemmProblem* sp, int np, int t, int& pi, int& z, int& tm, int& tn) {
+    if (sp[0].a_shared) {
+        // row block tm, then the column tiles of every problem in turn
+        const int tn_total = sp[np - 1].tn_off + sp[np - 1].tiles_n;
+        tm = t / tn_total;
+        const int c = t - tm * tn_total;
+        pi = 0;
+        while (pi + 1 < np && c >= sp[pi + 1].tn_off) ++pi;
+        tn = c - sp[pi].tn_off;
+        z = 0;
+        return;
+    }
     pi = 0;
     while (pi + 1 < np && t >= sp[pi + 1].tile_begin) ++pi;
     const GemmProblem& q = sp[pi];
@@ -514,7 +525,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         const int pb = P.phase_prob[ph], np = P.phase_prob[ph + 1] - pb;
         const GemmProblem* sp = sProb + (ph & 1) * kPhaseProbs;
         const int t_begin = sp[0].tile_begin;
-        const int t_end = sp[np - 1].tile_begin + sp[np - 1].tiles_per_batch * sp[np - 1].batch;
+        const int t_end = sp[0].a_shared ? sp[0].tiles_m * (sp[np - 1].tn_off + sp[np - 1].tiles_n)
+                                         : sp[np - 1].tile_begin + sp[np - 1].tiles_per_batch * sp[np - 1].batch;
         ok = ok && !*abort_flag;
         if (warp == 0) {
             // ---------------- TMA producer ----------------

@@ -41,6 +41,8 @@ struct GemmProblem {
     int b_mn, sym, out_kind, vec_ok;  // out_kind: kOutBF16 / kOutF32 / kOutF16
     int ab_f16;
     int bulk_st;  // non-symmetric 16-bit output written by TMA tensor stores through tmC
+    int a_shared; // the phase's problems share A: tiles go row block by row block across them
+    int tn_off;   // a_shared: this problem's first column tile in the row block
     int tiles_m, tiles_n, tiles_per_batch, tile_begin;
     void* out;
     long long out_ld, out_bstride;
@@ -70,6 +72,7 @@ struct GemmParamsT {
     int nprob, total_tiles;
     int bn;      // output tile width of the launch: 256 (default when 0) or 128
     int tile_m;  // output tile height: 128 (one CTA, default when 0) or 256 (a CTA pair)
+    int a_shared;  // single-phase launch whose problems share A (same rows, batch 1, not symmetric)
     int nphase;
     int phase_prob[kMaxPhases + 1];
     unsigned* grid_bar;
