@@ -17,7 +17,10 @@
 namespace mc {
 
 constexpr int kAStageBytes = kBM * kBK * 2;  // 16 KB
-constexpr int kGemmThreads = 192;
+// warp 0 and warp 6: TMA producers (even and odd K blocks: one thread issues
+// TMA loads at about half the rate two threads in different warps reach);
+// warp 1: MMA issuer; warps 2..5: epilogue
+constexpr int kGemmThreads = 224;
 // epilogue staging: each epilogue warp stages a 32 x 64 chunk of 16-bit
 // values in rows of 72 elements (144 B: 16-byte accesses are bank-conflict
 // free) so that every global load/store of the epilogue is a coalesced
@@ -528,8 +531,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         const int t_end = sp[0].a_shared ? sp[0].tiles_m * (sp[np - 1].tn_off + sp[np - 1].tiles_n)
                                          : sp[np - 1].tile_begin + sp[np - 1].tiles_per_batch * sp[np - 1].batch;
         ok = ok && !*abort_flag;
-        if (warp == 0) {
-            // ---------------- TMA producer ----------------
+        if (warp == 0 || warp == 6) {
+            // ---------------- TMA producers ----------------
+            // both walk every K block; warp 0 issues the even ones, warp 6 the
+            // odd ones (an even stage count gives each stage one producer)
+            static_assert(STAGES % 2 == 0, "stages split between two producers");
+            const int pid = warp == 6 ? 1 : 0;
             if (lane == 0 && ok) {
                 for (int t = t_begin + unit; t < t_end && ok; t += nunits) {
                     int pi, z, tm, tn;
@@ -539,6 +546,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                     const CUtensorMap* tmB = &P.p[pb + pi].tmB;
                     const int nk = (q.K + kBK - 1) / kBK;
                     for (int kb = 0; kb < nk; ++kb) {
+                        if ((stage & 1) != pid) {  // the other producer's stage
+                            if (++stage == kGemmStages) {
+                                stage = 0;
+                                phase ^= 1;
+                            }
+                            continue;
+                        }
                         if (!mbar_wait(&tail->empty[stage], phase ^ 1, abort_flag, P.status)) {
                             ok = false;
                             break;
@@ -634,7 +648,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                     aphase ^= 1;
                 }
             }
-        } else {
+        } else if (warp <= 5) {
             // ---------------- epilogue (warps 2..5) ----------------
             const int quarter = warp & 3;  // TMEM lanes this warp may access
             uint16_t* S = sEpi + (warp - 2) * (kEpiWarpBytes / 2);
@@ -687,7 +701,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         if (ph + 1 < P.nphase) grid_sync(P, nsync++, abort_flag, ph + 1, sProb + ((ph + 1) & 1) * kPhaseProbs);
     }
 
-    if (warp == 0 && lane == 0 && leader) {
+    if ((warp == 0 || warp == 6) && lane == 0 && leader) {
         // wait for the copies still in flight before exit (a pair's copies all
         // complete on the leader's barriers; the final cluster barrier keeps
         // the other CTA resident until then)

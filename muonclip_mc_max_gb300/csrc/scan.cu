@@ -25,12 +25,16 @@
 
 namespace mc {
 
-constexpr int kScanStages = 4;
+// Shared memory: a 1 KB block with the barriers, two Q buffers of nkb 16 KB
+// blocks each, then as many 32 KB K stages as fit in 224 KB: 6 at d = 64
+// (more K tiles in flight), 4 at d = 192.
+constexpr int kScanMaxStages = 6;
 constexpr int kScanQBlocks = 3;                  // d up to 192 per Q buffer
+constexpr int kScanRing = 224 * 1024;            // Q buffers + K stages
 constexpr int kQBlockBytes = kBM * kBK * 2;      // 16 KB
 constexpr int kKStageBytes = kBN * kBK * 2;      // 32 KB
 constexpr int kScanThreads = 192;
-constexpr int kScanSmem = 2 * kScanQBlocks * kQBlockBytes + kScanStages * kKStageBytes + 1024 + 256;
+constexpr int kScanSmem = 1024 + 1024 + kScanRing;
 
 struct ScanParams {
     CUtensorMap tmQ;   // {q_ld, T, B}, box {64, 128}
@@ -39,7 +43,8 @@ struct ScanParams {
     int B, T, H, causal;
     int q_head_stride, k_head_stride, nkb_main, nkb_rope, kr_col;
     int n_it, total_items;
-    int band;  // (sequence, head) pairs per band of the item order
+    int band;    // (sequence, head) pairs per band of the item order
+    int stages;  // K stages in the ring
     unsigned* keys;
     unsigned* done;  // zeroed counter of finished CTAs
     float sqrt_d;
@@ -50,8 +55,8 @@ struct ScanParams {
 };
 
 struct ScanSmemTail {
-    uint64_t kfull[kScanStages];
-    uint64_t kempty[kScanStages];
+    uint64_t kfull[kScanMaxStages];
+    uint64_t kempty[kScanMaxStages];
     uint64_t qfull[2], qempty[2];
     uint64_t tfull[2];
     uint64_t tempty[2];
@@ -106,16 +111,18 @@ MC_D int item_of_round(int r) {
 __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(const __grid_constant__ ScanParams P) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sQ = smem;
-    uint8_t* sK = smem + 2 * kScanQBlocks * kQBlockBytes;
-    ScanSmemTail* tail = reinterpret_cast<ScanSmemTail*>(sK + kScanStages * kKStageBytes);
+    static_assert(sizeof(ScanSmemTail) <= 1024, "tail");
+    ScanSmemTail* tail = reinterpret_cast<ScanSmemTail*>(smem);
+    const int nkb = P.nkb_main + P.nkb_rope;
+    const int nst = P.stages;
+    uint8_t* sQ = smem + 1024;                        // Q buffer qb, block kb: sQ + (qb * nkb + kb) * 16 KB
+    uint8_t* sK = sQ + 2 * nkb * kQBlockBytes;
     volatile int* abort_flag = &tail->abort_flag;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int nkb = P.nkb_main + P.nkb_rope;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kScanStages; ++s) {
+        for (int s = 0; s < nst; ++s) {
             mbar_init(&tail->kfull[s], 1);
             mbar_init(&tail->kempty[s], 1);
         }
@@ -150,7 +157,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(const __grid_cons
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t issued[kScanStages] = {0, 0, 0, 0};
+            uint32_t issued[kScanMaxStages] = {0, 0, 0, 0, 0, 0};
             uint32_t n = 0;  // items started by this CTA: Q buffer n & 1
             bool ok = true;
             for (int r = 0, i = item_of_round(0); i < P.total_items && ok; i = item_of_round(++r), ++n) {
@@ -160,7 +167,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(const __grid_cons
                 if (!mbar_wait(&tail->qempty[qb], ((n >> 1) & 1) ^ 1, abort_flag, P.status)) break;
                 mbar_arrive_expect_tx(&tail->qfull[qb], nkb * kQBlockBytes);
                 for (int kb = 0; kb < nkb; ++kb)
-                    tma_load_3d(sQ + (qb * kScanQBlocks + kb) * kQBlockBytes, &P.tmQ, &tail->qfull[qb],
+                    tma_load_3d(sQ + (qb * nkb + kb) * kQBlockBytes, &P.tmQ, &tail->qfull[qb],
                                 h * P.q_head_stride + kb * kBK, it * kBM, b);
                 for (int jt = 0; jt < njt && ok; ++jt) {
                     for (int kb = 0; kb < nkb; ++kb) {
@@ -176,7 +183,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(const __grid_cons
                             tma_load_3d(sK + stage * kKStageBytes, &P.tmKR, &tail->kfull[stage],
                                         P.kr_col, jt * kBN, b);
                         ++issued[stage];
-                        if (++stage == kScanStages) {
+                        if (++stage == nst) {
                             stage = 0;
                             phase ^= 1;
                         }
@@ -184,7 +191,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(const __grid_cons
                 }
             }
             volatile int never = 0;
-            for (int s = 0; s < kScanStages; ++s)
+            for (int s = 0; s < nst; ++s)
                 if (issued[s]) mbar_wait(&tail->kfull[s], (issued[s] - 1) & 1, &never, P.status);
             // Q buffer qb was last filled by item n-1 (qb = (n-1)&1) or n-2
             for (uint32_t j = (n > 2 ? n - 2 : 0); j < n; ++j)
@@ -200,7 +207,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(const __grid_cons
             int b, h, it, njt;
             decode_item(P, i, b, h, it, njt);
             const int qb = n & 1;
-            const uint32_t q0 = smem_u32(sQ + qb * kScanQBlocks * kQBlockBytes);
+            const uint32_t q0 = smem_u32(sQ + qb * nkb * kQBlockBytes);
             if (!mbar_wait(&tail->qfull[qb], (n >> 1) & 1, abort_flag, P.status)) break;
             tc_fence_after();
             for (int jt = 0; jt < njt && ok; ++jt) {
@@ -226,7 +233,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(const __grid_cons
                         umma_commit(&tail->kempty[stage]);
                     }
                     __syncwarp();
-                    if (++stage == kScanStages) {
+                    if (++stage == nst) {
                         stage = 0;
                         phase ^= 1;
                     }
@@ -379,6 +386,7 @@ cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream) {
     if (grid > P.total_items) grid = P.total_items;
     // about two rounds of items per band
     P.band = std::max(1, std::min(a.B * a.H, (2 * grid + P.n_it - 1) / P.n_it));
+    P.stages = std::min(kScanMaxStages, (kScanRing - 2 * nkb * kQBlockBytes) / kKStageBytes);
     TraceScope ts("scan", stream);
     return launch_pdl(scan_kernel, dim3(grid), dim3(kScanThreads), kScanSmem, stream, P);
 }
