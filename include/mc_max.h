@@ -220,9 +220,11 @@ size_t mc_muon_workspace_size(const int* rows, const int* cols, int count);
  *   in[i]   device f32 [rows[i]][cols[i]]   (host array of device pointers)
  *   out[i]  device f32 [rows[i]][cols[i]]   (may not alias in[i])
  * The three products per step run on tcgen05 tensor cores with bf16
- * operands and fp32 accumulation (X, A and B held in bf16); the Gram
- * matrix and A A use only the upper tiles (both are symmetric).
- * Requires cols % 4 == 0 and 16-byte aligned pointers.
+ * operands and fp32 accumulation (X, A and B held in bf16); for large
+ * batches the Gram matrix and A A use only the upper tiles (both are
+ * symmetric).  Any shape; pointers must be 4-byte aligned (float).  Rows
+ * with cols % 4 == 0 and 16-byte aligned pointers are read and written
+ * with 16-byte vectors, other shapes element by element.
  */
 mc_status mc_newton_schulz(const float* const* in, float* const* out, const int* rows,
                            const int* cols, int count, int steps, float a, float b, float c,

@@ -203,6 +203,7 @@ struct Carve {
 };
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+static bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; }
 
 // Projection D = A W with W [K][N] row-major (the MN-major B operand);
 // A and W both bf16 (f16 = 0) or both fp16 (f16 = 1); D stored in fp16.
@@ -692,7 +693,7 @@ bool plan_ns(const int* rows, const int* cols, int count, uint8_t* base, NsPlan&
 bool valid_mats(const int* rows, const int* cols, int count) {
     if (!rows || !cols || count <= 0) return false;
     for (int i = 0; i < count; ++i) {
-        if (rows[i] <= 0 || cols[i] <= 0 || cols[i] % 4) return false;
+        if (rows[i] <= 0 || cols[i] <= 0) return false;
         if ((int64_t)rows[i] * cols[i] > ((int64_t)1 << 31)) return false;
     }
     return true;
@@ -738,6 +739,10 @@ mc_status run_mat_pass(const NsPlan& P, int mode, float* const* w, const float* 
             tiles += (gr.m_pad / 64) * (gr.n_pad / 64);
             d.w = w[i];
             d.rms = rms_coef * sqrtf((float)std::max(rows[i], cols[i]));
+            // float4 accesses need whole 16-byte groups of columns on every row
+            d.vec = cols[i] % 4 == 0 &&
+                    (mode == 0 ? aligned16(m[i]) && aligned16(g[i])
+                               : mode == 1 ? aligned16(in[i]) : aligned16(w[i]));
             if (mode == 0) {
                 d.m = m[i];
                 d.g = g[i];
@@ -908,10 +913,10 @@ mc_status muon_impl(bool step, float* const* w, const float* const* g, float* co
     for (int i = 0; i < count; ++i) {
         if (step) {
             if (!w || !g || !m || !w[i] || !g[i] || !m[i]) return MC_ERR_INVALID_ARG;
-            if (!aligned16(w[i]) || !aligned16(g[i]) || !aligned16(m[i])) return MC_ERR_INVALID_ARG;
+            if (!aligned4(w[i]) || !aligned4(g[i]) || !aligned4(m[i])) return MC_ERR_INVALID_ARG;
         } else {
             if (!in || !out || !in[i] || !out[i]) return MC_ERR_INVALID_ARG;
-            if (!aligned16(in[i]) || !aligned16(out[i]) || in[i] == out[i]) return MC_ERR_INVALID_ARG;
+            if (!aligned4(in[i]) || !aligned4(out[i]) || in[i] == out[i]) return MC_ERR_INVALID_ARG;
         }
     }
     NsPlan P;

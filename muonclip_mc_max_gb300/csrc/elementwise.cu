@@ -230,7 +230,27 @@ __global__ void __launch_bounds__(kMatThreads) mat_pass_kernel(const __grid_cons
                     const int lr = p * 16 + (tid >> 4), lc = (tid & 15) * 4;
                     const int r = sr0 + lr, c = sc0 + lc;
                     float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (r < d.rows && c < d.cols) {
+                    if (r < d.rows && c < d.cols && !d.vec) {
+                        // any width: element by element, zero past the last column
+                        float uu[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            uu[k] = 0.f;
+                            if (c + k < d.cols) {
+                                const size_t off = (size_t)r * d.cols + c + k;
+                                float mv = d.m[off];
+                                if (B.mode == 0) {
+                                    const float gv = d.g[off];
+                                    mv = __fmaf_rn(B.mu, mv, gv);
+                                    d.m[off] = mv;
+                                    uu[k] = B.nesterov ? __fmaf_rn(B.mu, mv, gv) : mv;
+                                } else {
+                                    uu[k] = mv;
+                                }
+                            }
+                        }
+                        u = make_float4(uu[0], uu[1], uu[2], uu[3]);
+                    } else if (r < d.rows && c < d.cols) {
                         const size_t off = (size_t)r * d.cols + c;
                         float4 mv = *reinterpret_cast<const float4*>(d.m + off);
                         if (B.mode == 0) {
@@ -308,7 +328,18 @@ __global__ void __launch_bounds__(kMatThreads) mat_pass_kernel(const __grid_cons
 #pragma unroll
                     for (int k = 0; k < 4; ++k) o[k] = osc * (d.tr ? U[lc + k][lr] : U[lr][lc + k]);
                     const size_t off = (size_t)r * d.cols + c;
-                    if (B.mode == 2) {
+                    if (!d.vec) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            if (c + k >= d.cols) break;
+                            if (B.mode == 2) {
+                                const float w = d.w[off + k];
+                                d.w[off + k] = w - B.lr * (d.rms * o[k] + B.wd * w);
+                            } else {
+                                d.w[off + k] = o[k];
+                            }
+                        }
+                    } else if (B.mode == 2) {
                         float4 w = *reinterpret_cast<const float4*>(d.w + off);
                         // W - lr (rms O + wd W), each step rounded as written
                         w.x = w.x - B.lr * (d.rms * o[0] + B.wd * w.x);

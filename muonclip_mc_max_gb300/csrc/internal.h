@@ -198,6 +198,7 @@ struct MatDesc {
     const float* oscale; // modes 2/3: optional device scale of O (zero NS steps)
     float rms;           // mode 2: rms_coef * sqrt(max(rows, cols))
     int rows, cols, tr;  // tr: X = transpose of the matrix (rows > cols)
+    int vec;             // cols % 4 == 0 and 16-byte aligned rows: float4 accesses
     int m_pad, n_pad;
     int tiles_x, tile_begin;  // 64 x 64 tiles over X [m_pad][n_pad]
 };

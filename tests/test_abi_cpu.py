@@ -49,11 +49,15 @@ def test_invalid_arguments_rejected_on_host(lib):
     # bad dtype
     assert lib.mc_max_logits_mha(fake, fake, fake, 7, 2, 8, 64, 1, 64, 0, 0, fake, nil, ws,
                                  1 << 30, nil) == 1
-    # Muon: cols not a multiple of 4, empty batch
+    # Muon: a zero-size matrix, a pointer that is not float-aligned, an empty batch
     rows = (ctypes.c_int * 1)(8)
-    cols = (ctypes.c_int * 1)(6)
+    cols = (ctypes.c_int * 1)(0)
     ptrs = (ctypes.c_void_p * 1)(4096)
     assert lib.mc_muon_step(ptrs, ptrs, ptrs, rows, cols, 1, 1e-3, 0.95, 0.1, 0.2, 5, 3.4, -4.7,
+                            2.0, 1e-7, 0, ws, 1 << 30, nil) == 1
+    cols = (ctypes.c_int * 1)(6)
+    odd = (ctypes.c_void_p * 1)(4098)
+    assert lib.mc_muon_step(odd, odd, odd, rows, cols, 1, 1e-3, 0.95, 0.1, 0.2, 5, 3.4, -4.7,
                             2.0, 1e-7, 0, ws, 1 << 30, nil) == 1
     assert lib.mc_newton_schulz(ptrs, ptrs, rows, cols, 0, 5, 3.4, -4.7, 2.0, 1e-7, ws, 1 << 30,
                                 nil) == 1
