@@ -63,6 +63,8 @@ def load():
     lib.oracle_max_logits_mla.argtypes = [_dp, I, I, I, _dp, I, _dp, _dp, I, _dp,
                                           I, I, I, D, I, _ip, I, _ip, I, _dp]
     lib.oracle_max_logits_mla.restype = I
+    lib.oracle_attention_mha.argtypes = [_dp, _dp, _dp, I, I, I, I, I, _dp, _dp]
+    lib.oracle_attention_mha.restype = I
     lib.oracle_gamma.argtypes = [_fp, I, F, _fp, _fp]
     lib.oracle_gamma.restype = None
     lib.oracle_qk_clip_mha.argtypes = [V, V, I, I, I, I, _fp, F, _fp]
@@ -177,6 +179,24 @@ def max_logits_mla(x, w_qa, w_qb, w_kva, w_kb, H: int, nope: int, rope: int,
 # ---------------------------------------------------------------------------
 # (2) gamma and QK-Clip
 # ---------------------------------------------------------------------------
+
+def attention_mha(q, k, v, H: int, dh: int, causal: bool = False):
+    """Softmax attention forward in fp64 with the max logit taken along.
+
+    q, k, v [B, T, H*dh] (head h = column block h).  Returns (o [B, T, H*dh],
+    s_bh [B, H]) with s_bh = max_{i,j} q_i.k_j / sqrt(dh) over allowed pairs."""
+    lib = load()
+    Q, K, V = _to_f64(q), _to_f64(k), _to_f64(v)
+    B, T, W = Q.shape
+    assert W == H * dh and K.shape == Q.shape and V.shape == Q.shape
+    o = np.empty_like(Q)
+    s = np.empty((B, H))
+    rc = lib.oracle_attention_mha(_ptr(Q), _ptr(K), _ptr(V), B, T, H, dh, int(causal), _ptr(o),
+                                  _ptr(s))
+    if rc:
+        raise RuntimeError(f"oracle_attention_mha failed ({rc})")
+    return o, s
+
 
 def gamma(s_max, tau: float):
     """(gamma, sqrt_gamma) as float32 arrays from float32 S_max."""
@@ -354,6 +374,27 @@ def max_logits_mla_np(x, w_qa, w_qb, w_kva, w_kb, H, nope, rope, rope_base, caus
             k = np.concatenate([kc, kr], axis=1)
             out[ib, ih] = _pair_max(q, k, causal) / np.sqrt(qk)
     return out
+
+
+def attention_mha_np(q, k, v, H: int, dh: int, causal: bool = False, batches=None, heads=None):
+    """As attention_mha, with library GEMMs (fp64), for the listed
+    (batch, head) pairs: returns (o [nb, T, nh, dh], s_bh [nb, nh])."""
+    Q, K, V = _to_f64(q), _to_f64(k), _to_f64(v)
+    B, T, _ = Q.shape
+    batches = list(range(B)) if batches is None else list(batches)
+    heads = list(range(H)) if heads is None else list(heads)
+    o = np.empty((len(batches), T, len(heads), dh))
+    s_bh = np.empty((len(batches), len(heads)))
+    mask = np.tril(np.ones((T, T), dtype=bool)) if causal else np.ones((T, T), dtype=bool)
+    for ib, b in enumerate(batches):
+        for ih, h in enumerate(heads):
+            cols = slice(h * dh, (h + 1) * dh)
+            s = (Q[b][:, cols] @ K[b][:, cols].T) / np.sqrt(dh)
+            s = np.where(mask, s, -np.inf)
+            s_bh[ib, ih] = s.max()
+            p = np.exp(s - s.max(axis=1, keepdims=True))
+            o[ib, :, ih] = (p @ V[b][:, cols]) / p.sum(axis=1, keepdims=True)
+    return o, s_bh
 
 
 def newton_schulz_np(g, steps: int = 5, coeffs=NS_COEFFS, eps: float = 1e-7) -> np.ndarray:

@@ -38,6 +38,11 @@
  *   - Newton-Schulz: X0 = U / (||U||_F + eps); transpose when rows > cols;
  *     X <- aX + (b A + c A A) X with A = X X^T.
  *
+ *   - Attention forward (the row that takes the max logit inside the forward
+ *     pass): O_i = sum_j softmax_j(s_ij / sqrt(dh)) v_j with s_ij = q_i . k_j
+ *     over the keys j the mask allows ([K2-zh 2.1] calls S the largest
+ *     softmax input: the logits are the inputs of this softmax).
+ *
  * Parity status: every function here is pinned by the CPU tests against
  * closed forms, special cases, library routines or brute force (see
  * tests/test_oracle_pins.py).
@@ -236,6 +241,65 @@ int oracle_max_logits_mla(const double* x, int B, int T, int D,
         }
     }
     free(cq); free(ckv); free(qh); free(kc);
+    return ORACLE_OK;
+}
+
+/*
+ * Softmax attention forward of an MHA layer, with the max logit taken on
+ * the way.  For each sequence b, head h and query i:
+ *   s_ij = q_i . k_j for the keys j the mask allows (j <= i when causal),
+ *   O_i  = sum_j exp(s_ij / sqrt(dh) - m_i) v_j / sum_j exp(s_ij / sqrt(dh) - m_i),
+ *          m_i = max_j s_ij / sqrt(dh) (the usual shift; the ratio is the softmax),
+ *   S_bh = max_{i,j} s_ij / sqrt(dh): the same max logit as
+ *          oracle_max_logits_mha, taken here from the given q and k.
+ * q, k, v, o [B][T][H*dh] (head h = columns [h*dh, (h+1)*dh)); s_bh [B][H].
+ * A NaN logit makes S_bh NaN (like a tensor max) and the row's output NaN.
+ */
+int oracle_attention_mha(const double* q, const double* k, const double* v, int B, int T, int H,
+                         int dh, int causal, double* o, double* s_bh) {
+    if (B <= 0 || T <= 0 || H <= 0 || dh <= 0) return ORACLE_ERR_ARG;
+    const long ld = (long)H * dh;
+    const double scale = 1.0 / sqrt((double)dh);
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < H; ++h) {
+            double best = -INFINITY;
+            int saw_nan = 0;
+#pragma omp parallel for schedule(dynamic, 4) reduction(max : best) reduction(| : saw_nan)
+            for (long i = 0; i < T; ++i) {
+                const double* qi = q + ((long)b * T + i) * ld + (long)h * dh;
+                const long jend = causal ? i + 1 : T;
+                double* s = (double*)malloc(sizeof(double) * (size_t)jend);
+                double m = -INFINITY;
+                int row_nan = 0;
+                for (long j = 0; j < jend; ++j) {
+                    const double* kj = k + ((long)b * T + j) * ld + (long)h * dh;
+                    double d = 0.0;
+                    for (int f = 0; f < dh; ++f) d += qi[f] * kj[f];
+                    s[j] = d * scale;
+                    if (isnan(d)) row_nan = 1;
+                    else if (s[j] > m) m = s[j];
+                }
+                double* oi = o + ((long)b * T + i) * ld + (long)h * dh;
+                if (row_nan) {
+                    saw_nan = 1;
+                    for (int f = 0; f < dh; ++f) oi[f] = NAN;
+                } else {
+                    if (m > best) best = m;
+                    double l = 0.0;
+                    for (int f = 0; f < dh; ++f) oi[f] = 0.0;
+                    for (long j = 0; j < jend; ++j) {
+                        const double p = exp(s[j] - m);
+                        const double* vj = v + ((long)b * T + j) * ld + (long)h * dh;
+                        l += p;
+                        for (int f = 0; f < dh; ++f) oi[f] += p * vj[f];
+                    }
+                    for (int f = 0; f < dh; ++f) oi[f] /= l;
+                }
+                free(s);
+            }
+            s_bh[(long)b * H + h] = saw_nan ? NAN : best;
+        }
+    }
     return ORACLE_OK;
 }
 

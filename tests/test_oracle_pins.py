@@ -505,3 +505,83 @@ def test_np_muon_matches_c_oracle(shape):
             np.testing.assert_allclose(v, u, rtol=1e-10, atol=1e-13)
     np.testing.assert_allclose(oracle.newton_schulz_np(g, 3), oracle.newton_schulz(g, 3),
                                rtol=1e-10, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# attention forward with the max logit taken along
+# ---------------------------------------------------------------------------
+
+def _qkv(B, T, H, dh, seed, scale=1.0):
+    rng = np.random.default_rng(seed)
+    return [rng.standard_normal((B, T, H * dh)) * scale for _ in range(3)]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_c_matches_library_gemm_formulation(causal):
+    q, k, v = _qkv(2, 13, 3, 8, 1101)
+    o, s = oracle.attention_mha(q, k, v, 3, 8, causal)
+    o2, s2 = oracle.attention_mha_np(q, k, v, 3, 8, causal)
+    assert np.abs(o.reshape(2, 13, 3, 8) - o2).max() < 1e-12
+    assert np.abs(s - s2).max() < 1e-12
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_zero_queries_average_the_values(causal):
+    """q = 0: every logit is 0, the softmax is uniform over the allowed keys,
+    so O_i is the mean of v_0..v_{i} (causal) or of all v (not causal)."""
+    _, k, v = _qkv(1, 11, 2, 4, 1102)
+    q = np.zeros_like(k)
+    o, s = oracle.attention_mha(q, k, v, 2, 4, causal)
+    for i in range(11):
+        n = i + 1 if causal else 11
+        assert np.allclose(o[0, i], v[0, :n].mean(axis=0), atol=1e-14)
+    assert np.all(s == 0.0)
+
+
+def test_attention_single_key_returns_its_value():
+    q, k, v = _qkv(3, 1, 2, 8, 1103)
+    o, s = oracle.attention_mha(q, k, v, 2, 8, True)
+    assert np.array_equal(o, v)
+    ref = (q.reshape(3, 1, 2, 8) * k.reshape(3, 1, 2, 8)).sum(-1)[:, 0] / np.sqrt(8)
+    assert np.allclose(s, ref, atol=1e-14)
+
+
+def test_attention_is_invariant_to_key_order():
+    """Without a mask, permuting the (key, value) pairs leaves O and S alone."""
+    q, k, v = _qkv(1, 9, 1, 8, 1104)
+    perm = np.random.default_rng(5).permutation(9)
+    o, s = oracle.attention_mha(q, k, v, 1, 8, False)
+    o2, s2 = oracle.attention_mha(q, k[:, perm], v[:, perm], 1, 8, False)
+    assert np.allclose(o, o2, atol=1e-13) and np.allclose(s, s2, atol=1e-13)
+
+
+def test_attention_dominant_key_selects_its_value():
+    """A logit 60 above all others puts weight > 1 - 1e-20 on its key."""
+    q, k, v = _qkv(1, 6, 1, 4, 1105, scale=0.01)
+    k[0, 3] = 0.0
+    k[0, 3, 0] = 1.0
+    q[0, :, :] = 0.0
+    q[0, :, 0] = 60.0 * 2.0   # q.k_3 / sqrt(4) = 60; every other logit is ~0
+    o, _ = oracle.attention_mha(q, k, v, 1, 4, False)
+    assert np.allclose(o[0], np.broadcast_to(v[0, 3], (6, 4)), atol=1e-20 * np.abs(v).max() + 1e-24)
+
+
+def test_attention_max_logit_equals_the_scan_oracle():
+    """S from the attention oracle on q = x W_q, k = x W_k is the max logit
+    of oracle_max_logits_mha on (x, W_q, W_k)."""
+    inp = mc_inputs.mha_layer(B=2, T=40, D=24, H=3, dh=8, n_hot=1, seed=1106, muon=False,
+                              w_std=0.3)
+    x = inp["x"].double().numpy()
+    wq, wk = inp["wq"].double().numpy(), inp["wk"].double().numpy()
+    q, k = x @ wq, x @ wk
+    for causal in (False, True):
+        _, s = oracle.attention_mha(q, k, np.zeros_like(q), 3, 8, causal)
+        ref = oracle.max_logits_mha(inp["x"], inp["wq"], inp["wk"], 3, 8, causal)
+        assert np.allclose(s, ref, rtol=1e-12, atol=0)
+
+
+def test_attention_nan_logit_propagates():
+    q, k, v = _qkv(1, 5, 1, 4, 1107)
+    q[0, 2, 1] = np.nan
+    o, s = oracle.attention_mha(q, k, v, 1, 4, True)
+    assert np.isnan(s).all() and np.isnan(o[0, 2]).all() and np.isfinite(o[0, 1]).all()
