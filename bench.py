@@ -9,7 +9,7 @@ the library's C ABI.  Default workload: an MHA layer in bf16, x [8, 1024,
 W_q and W_k.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload c2|c3|c4|c5]
+                  [--workload c2|c3|c4|c5|attn|attnl]
 
 value     = algorithmic TFLOP/s of the step (scan + Newton-Schulz flops per
             step / device time per step, inputs resident, L2 flushed between
@@ -20,6 +20,10 @@ roofline  = the dominant kernel's algorithmic work per launch / its
             event-timed duration against the measured peak;
 cpu_baseline = the fp64 oracle on this host's cores on a bounded sample.
 --impl reference times that oracle (the only reference this method has).
+
+attn / attnl time the attention forward that takes the max logit along
+(value = its algorithmic TFLOP/s: 4 flops per allowed (i, j) pair and head
+dimension); they are extra lines, not the default workload.
 """
 from __future__ import annotations
 
@@ -312,8 +316,59 @@ class MlaLayer(Workload):
         return flops, dt, f"one head of the MLA scan over the first {T} tokens, fp64"
 
 
+class AttnLayer(Workload):
+    """attn / attnl: the attention forward with the max logit taken along."""
+
+    def __init__(self, which="attn"):
+        self.name = which
+        if which == "attn":
+            self.B, self.T, self.H, self.dh, self.causal = 8, 1024, 16, 64, False
+        else:
+            self.B, self.T, self.H, self.dh, self.causal = 2, 8192, 16, 128, True
+        self.desc = (f"MHA attention forward bf16 q,k,v [{self.B},{self.T},{self.H}x{self.dh}] "
+                     f"{'causal' if self.causal else 'non-causal'}, O bf16 and the per-head max logit")
+        pairs = scan_pairs(self.B, self.T, self.causal)
+        self.units = {"attn": ("tensor", 4 * pairs * self.H * self.dh)}
+        self.metric = "attention forward with the max logit taken along, TFLOP/s (% bf16 peak)"
+        self.scan_flops = self.units["attn"][1]
+        self.ns_flops = 0
+
+    def make(self, device):
+        import torch
+        s = mc_inputs.attention_qkv(self.B, self.T, self.H, self.dh, seed=1500, device=device)
+        s["o"] = torch.empty_like(s["q"])
+        s["s_max"] = torch.empty(self.H, dtype=torch.float32, device=device)
+        return s
+
+    def inputs(self, s):
+        return [s["q"], s["k"], s["v"]]
+
+    def outputs(self, s):
+        return [s["s_max"]]
+
+    def step(self, s, api):
+        self.step_part(s, api, "scan")
+
+    def step_part(self, s, api, part):
+        if part == "scan":
+            api.mc_attention_mha(s["q"], s["k"], s["v"], self.H, self.dh, causal=self.causal, out=s["o"],
+                                 s_max=s["s_max"])
+
+    def oracle_sample(self, s):
+        import oracle
+        T = min(self.T, 512)
+        cols = slice(0, self.dh)
+        q, k, v = (s[n][:1, :T, cols].cpu() for n in ("q", "k", "v"))
+        t0 = time.perf_counter()
+        oracle.attention_mha(q, k, v, 1, self.dh, self.causal)
+        dt = time.perf_counter() - t0
+        return (4 * scan_pairs(1, T, self.causal) * self.dh, dt,
+                f"one head of one sequence over the first {T} tokens, fp64")
+
+
 WORKLOADS = {"c2": lambda: MhaLayer(), "c4": lambda: ExpertBatch(), "c3": lambda: MlaLayer("c3"),
-             "c5": lambda: MlaLayer("c5")}
+             "c5": lambda: MlaLayer("c5"), "attn": lambda: AttnLayer("attn"),
+             "attnl": lambda: AttnLayer("attnl")}
 
 
 # ---------------------------------------------------------------------------
@@ -402,7 +457,7 @@ def run_reference(args, wl):
     tot = sum(times)
     value = flops * len(times) / tot / 1e12
     cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "impl": "reference",
+    line = {"metric": getattr(wl, "metric", METRIC), "value": value, "unit": "TFLOP/s", "impl": "reference",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * tot / len(times), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -600,7 +655,7 @@ def run_ours(args, wl):
                "cores": int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)),
                "kind": "oracle", "sample": f"{sample}; {reps} repetitions, {dt_tot:.1f} s"}
         line = {
-            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "metric": getattr(wl, "metric", METRIC), "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",

@@ -169,6 +169,33 @@ mc_status mc_max_logits_mla(const mc_mla_layer* layer, const void* x, int B, int
                             size_t ws_bytes, mc_stream_t stream);
 
 /* ======================================================================
+ * Attention forward with the max logit taken along
+ * ====================================================================== */
+
+/*
+ * Softmax attention forward of an MHA layer that also yields the per-head
+ * max logit of the MuonClip step ("Kimi K2" section 2.1: S_max^h is the
+ * largest softmax input; the K2 notes: the clip uses this step's max logit
+ * and leaves the forward itself unchanged), so S_max costs one max per logit
+ * of the forward:
+ *   O_i = sum_j softmax_j(q_i . k_j / sqrt(dh)) v_j   (j <= i when causal),
+ *   s_max[h] = max over sequences and (i, j) of q_i . k_j / sqrt(dh).
+ *   q, k, v   device bf16 [B][T][H*dh] (head h = columns [h*dh, (h+1)*dh))
+ *   o         device bf16 [B][T][H*dh], written (must not alias q, k, v)
+ *   s_max     device f32 [H]; accumulate != 0 max-merges into its contents
+ *   s_max_bh  optional device f32 [B][H] (per-sequence maxima), or NULL
+ * dh must be 64 or 128; pointers 16-byte aligned; T >= 1.  Tensor cores
+ * compute q.k and P.v with fp32 accumulation; the softmax weights P are
+ * rounded once to bf16 for P.v.  NaN logits make s_max NaN and set
+ * MC_DEV_NONFINITE.  ws: at least mc_attention_mha_workspace_size(B, H)
+ * bytes, 256-byte aligned.
+ */
+size_t mc_attention_mha_workspace_size(int B, int H);
+mc_status mc_attention_mha(const void* q, const void* k, const void* v, int B, int T, int H, int dh,
+                           int causal, int accumulate, void* o, float* s_max, float* s_max_bh,
+                           void* ws, size_t ws_bytes, mc_stream_t stream);
+
+/* ======================================================================
  * (2) QK-Clip
  * ====================================================================== */
 

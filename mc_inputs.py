@@ -187,3 +187,13 @@ def matrix(rows, cols, seed, device="cpu", std=1.0):
     """One N(0, std^2) fp32 matrix (Newton-Schulz and GEMM test inputs)."""
     g = _gen(seed, device)
     return _randn((rows, cols), g, device, std=std)
+
+
+def attention_qkv(B, T, H, dh, seed, device="cpu", q_std=1.0):
+    """bf16 q, k, v [B, T, H*dh], N(0, 1) (q scaled by q_std): the inputs of
+    the attention forward with the max logit taken along."""
+    g = _gen(seed, device)
+    q = _randn((B, T, H * dh), g, device, std=q_std).to(torch.bfloat16)
+    k = _randn((B, T, H * dh), g, device).to(torch.bfloat16)
+    v = _randn((B, T, H * dh), g, device).to(torch.bfloat16)
+    return {"q": q, "k": k, "v": v, "H": H, "dh": dh}

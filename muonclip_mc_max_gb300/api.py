@@ -88,6 +88,8 @@ def load_library():
         "mc_max_logits_mha_noalloc": ([V, V, V, I, I, I, I, I, I, I, I, V, V, V], I),
         "mc_max_logits_mla_workspace_size": ([ctypes.POINTER(MlaLayer), I, I], S),
         "mc_max_logits_mla": ([ctypes.POINTER(MlaLayer), V, I, I, I, I, V, V, V, S, V], I),
+        "mc_attention_mha_workspace_size": ([I, I], S),
+        "mc_attention_mha": ([V, V, V, I, I, I, I, I, I, V, V, V, V, S, V], I),
         "mc_qk_clip_mha": ([V, V, I, I, I, I, V, F, V, V], I),
         "mc_qk_clip_mla": ([ctypes.POINTER(MlaLayer), V, F, V, V], I),
         "mc_qk_clip_global": ([V, V, I, I, I, V, I, F, F, V, V], I),
@@ -200,6 +202,32 @@ def mc_max_logits_mha(x, wq, wk, H: int, dh: int, causal: bool = False, accumula
         _ptr(x), _ptr(wq), _ptr(wk), dt, B, T, D, H, dh, int(causal), int(accumulate),
         _ptr(s_max), _ptr(s_max_bh), ws, nb, _stream(stream)))
     return s_max
+
+
+def mc_attention_mha_workspace_size(B: int, H: int) -> int:
+    return load_library().mc_attention_mha_workspace_size(B, H)
+
+
+def mc_attention_mha(q, k, v, H: int, dh: int, causal: bool = False, accumulate: bool = False,
+                     out=None, s_max=None, s_max_bh=None, workspace=None, stream=None):
+    """q, k, v [B,T,H*dh] bf16.  Returns (o [B,T,H*dh] bf16, s_max [H] f32):
+    softmax attention with the per-head max logit taken along."""
+    lib = load_library()
+    _need_cuda(q, k, v, out, s_max, s_max_bh)
+    B, T, W = q.shape
+    if W != H * dh or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must all be [B, T, H*dh]")
+    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise ValueError("q, k, v must be bf16")
+    if out is None:
+        out = torch.empty_like(q)
+    if s_max is None:
+        s_max = torch.empty(H, dtype=torch.float32, device=q.device)
+    ws, nb = _ws(workspace, lib.mc_attention_mha_workspace_size(B, H), q.device)
+    _check("mc_attention_mha", lib.mc_attention_mha(
+        _ptr(q), _ptr(k), _ptr(v), B, T, H, dh, int(causal), int(accumulate), _ptr(out), _ptr(s_max),
+        _ptr(s_max_bh), ws, nb, _stream(stream)))
+    return out, s_max
 
 
 def mc_max_logits_mha_noalloc(x, wq, wk, H: int, dh: int, causal: bool = False,

@@ -16,7 +16,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _ROOT = os.path.dirname(_HERE)
 _CSRC = os.path.join(_HERE, "csrc")
 _BUILD = os.path.join(_ROOT, "_build", "mc_max")
-SOURCES = ["abi.cu", "gemm.cu", "scan.cu", "elementwise.cu"]
+SOURCES = ["abi.cu", "gemm.cu", "scan.cu", "elementwise.cu", "attn.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

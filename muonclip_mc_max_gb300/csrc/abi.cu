@@ -333,6 +333,44 @@ static size_t mha_carve(Carve& c, int B, int T, int D, int H, int dh, mc_dtype d
     return c.used;
 }
 
+size_t mc_attention_mha_workspace_size(int B, int H) {
+    if (B <= 0 || H <= 0) return 0;
+    return align256(sizeof(unsigned) * ((size_t)B * H + 1));
+}
+
+mc_status mc_attention_mha(const void* q, const void* k, const void* v, int B, int T, int H, int dh, int causal,
+                           int accumulate, void* o, float* s_max, float* s_max_bh, void* ws, size_t ws_bytes,
+                           mc_stream_t stream_) {
+    cudaStream_t stream = (cudaStream_t)stream_;
+    if (!q || !k || !v || !o || !s_max) return MC_ERR_INVALID_ARG;
+    if (B <= 0 || T <= 0 || H <= 0 || dh <= 0) return MC_ERR_INVALID_ARG;
+    if (dh != 64 && dh != 128) return MC_ERR_UNSUPPORTED;
+    if ((int64_t)B * T > INT32_MAX || (int64_t)H * dh > INT32_MAX) return MC_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return MC_ERR_INVALID_ARG;
+    if (o == q || o == k || o == v) return MC_ERR_INVALID_ARG;
+    const size_t need = mc_attention_mha_workspace_size(B, H);
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < need) return MC_ERR_WORKSPACE;
+    unsigned* keys = (unsigned*)ws;
+    MC_CUDA(cudaMemsetAsync(keys, 0, sizeof(unsigned) * ((size_t)B * H + 1), stream));
+    AttnArgs a;
+    memset(&a, 0, sizeof(a));
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.o = o;
+    a.B = B;
+    a.T = T;
+    a.H = H;
+    a.dh = dh;
+    a.causal = causal ? 1 : 0;
+    a.keys = keys;
+    a.accumulate = accumulate ? 1 : 0;
+    a.s_max = s_max;
+    a.s_bh = s_max_bh;
+    MC_CUDA(launch_attn(a, stream));
+    return MC_OK;
+}
+
 size_t mc_max_logits_mha_workspace_size(int B, int T, int D, int H, int dh, mc_dtype dtype) {
     if (B <= 0 || T <= 0 || D <= 0 || H <= 0 || dh <= 0) return 0;
     Carve c{nullptr, 0};

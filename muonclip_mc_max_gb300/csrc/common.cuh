@@ -325,6 +325,38 @@ MC_D float warp_max_nan(float v) {
     return v;
 }
 
+// S_max[h] = max over sequences of key / sqrt(d) (NaN propagates); the
+// per-sequence maxima are written too when s_bh is given.
+MC_D void finalize_head(const unsigned* keys, int B, int H, int h, float sqrt_d, int accumulate,
+                        float* s_max, float* s_bh, unsigned* status) {
+    unsigned best = 0;
+    for (int b = 0; b < B; ++b) {
+        unsigned k = __ldcg(keys + b * H + h);
+        if (s_bh) s_bh[b * H + h] = __fdiv_rn(key_float(k), sqrt_d);
+        best = max(best, k);
+    }
+    float s = __fdiv_rn(key_float(best), sqrt_d);
+    if (accumulate) s = max_nan(s_max[h], s);
+    if (!isfinite(s)) set_status(status, MC_DEV_NONFINITE);
+    s_max[h] = s;
+}
+
+// 32 lanes x 32 consecutive 32-bit columns from registers: thread i writes
+// lane (base + i); tmem_st_wait() before the columns are read or reused
+MC_D void tmem_st32(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+MC_D void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 #endif  // __CUDACC__
 
 }  // namespace mc

@@ -148,6 +148,20 @@ struct ScanArgs {
 };
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream);
 
+// Attention forward with the max logit taken along (attn.cu) -------------------
+struct AttnArgs {
+    const void* q;       // bf16 [B][T][H*dh]
+    const void* k;
+    const void* v;
+    void* o;             // bf16 [B][T][H*dh]
+    int B, T, H, dh, causal;
+    unsigned* keys;      // [B*H] zeroed monotonic keys, then a zeroed done counter
+    int accumulate;
+    float* s_max;
+    float* s_bh;
+};
+cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream);
+
 // fp32 CUDA-core fallbacks for small or unaligned MHA shapes
 cudaError_t launch_proj_simt(const void* x, const void* w, mc_dtype dt, float* out, int rows,
                              int D, int N, cudaStream_t stream);

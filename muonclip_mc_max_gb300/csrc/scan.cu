@@ -66,21 +66,6 @@ struct ScanSmemTail {
     int last_cta;
 };
 
-// S_max[h] = max over sequences of key / sqrt(d) (NaN propagates); the
-// per-sequence maxima are written too when s_bh is given.
-MC_D void finalize_head(const unsigned* keys, int B, int H, int h, float sqrt_d, int accumulate,
-                        float* s_max, float* s_bh, unsigned* status) {
-    unsigned best = 0;
-    for (int b = 0; b < B; ++b) {
-        unsigned k = __ldcg(keys + b * H + h);
-        if (s_bh) s_bh[b * H + h] = __fdiv_rn(key_float(k), sqrt_d);
-        best = max(best, k);
-    }
-    float s = __fdiv_rn(key_float(best), sqrt_d);
-    if (accumulate) s = max_nan(s_max[h], s);
-    if (!isfinite(s)) set_status(status, MC_DEV_NONFINITE);
-    s_max[h] = s;
-}
 
 // Item order: bands of P.band (sequence, head) pairs; within a band the
 // query tiles go heaviest causal tile first, pairs minor.  The items running
