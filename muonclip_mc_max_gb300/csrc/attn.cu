@@ -61,6 +61,14 @@ struct AttnSmemTail {
     int last_cta;
 };
 
+// 2^x with the hardware approximation (relative error about 2^-22, far below
+// the bf16 rounding of the softmax weights; tiny results flush to zero)
+MC_D float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 MC_D void attn_item(const AttnParams& P, int i, int& b, int& h, int& it, int& njb) {
     const int BH = P.B * P.H;
     const int per_band = P.band * P.n_it;
@@ -287,20 +295,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                     for (int e = 0; e < kAttnBlk; ++e)
                         if (key0 + e >= lim) v[e] = -INFINITY;
                 }
-                float mb = -INFINITY;
+                // four independent max chains (the row max), then one
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int e = 0; e < kAttnBlk; e += 2) mb = max3_nan(mb, v[e], v[e + 1]);
+                for (int e = 0; e < kAttnBlk; e += 8)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) m4[c] = max3_nan(m4[c], v[e + 2 * c], v[e + 2 * c + 1]);
+                const float mb = max_nan(max_nan(m4[0], m4[1]), max_nan(m4[2], m4[3]));
                 m_raw = max_nan(m_raw, mb);
-                // softmax in base 2: x = s log2(e) / sqrt(dh)
-                const float m_new = row_ok ? fmaxf(m, mb * P.scale_log2) : 0.f;
-                const float alpha = row_ok ? exp2f(m - m_new) : 1.f;
-                float lsum = 0.f;
+                // softmax in base 2: x = s log2(e) / sqrt(dh).  P, O and l are
+                // relative to the reference max m, which moves (and O with it)
+                // only when the row max exceeds it by more than 8: the weights
+                // stay below 2^8 and most blocks skip the rescale.
+                const float mx = mb * P.scale_log2;
+                const float m_new = !row_ok ? 0.f : (mx > m + 8.f || m == -INFINITY) ? fmaxf(m, mx) : m;
+                const float alpha = row_ok && m_new != m ? ex2_approx(m - m_new) : 1.f;
+                float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // eight partial sums
 #pragma unroll
                 for (int e = 0; e < kAttnBlk; ++e) {
-                    const float p = row_ok ? exp2f(__fmaf_rn(v[e], P.scale_log2, -m_new)) : 0.f;
+                    const float p = row_ok ? ex2_approx(__fmaf_rn(v[e], P.scale_log2, -m_new)) : 0.f;
                     v[e] = p;
-                    lsum += p;
+                    ls[e & 7] += p;
                 }
+                const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
                 l = __fmaf_rn(l, alpha, lsum);
                 m = m_new;
                 if (j >= 1) {
