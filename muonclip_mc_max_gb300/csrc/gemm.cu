@@ -1,12 +1,14 @@
 // gemm.cu -- persistent, warp-specialised tcgen05 GEMM for sm_103a.
 //
-// One CTA per SM walks a static round-robin list of 128 x 256 output tiles
-// drawn from up to four problems (projections of one layer, or one
-// Newton-Schulz phase over every matrix of a batch).
-//   warp 0      TMA producer: A tile 128 x 64 and B tile 256 x 64 (bf16,
-//               128-byte swizzle) per stage into a 4-stage ring
-//   warp 1      TMEM owner and MMA issuer: 4 x tcgen05.mma (K = 16) per
-//               stage into one of two 128 x 256 fp32 TMEM accumulators
+// Persistent CTAs (or CTA pairs) walk a static round-robin list of output
+// tiles drawn from up to four problems per phase (projections of one layer,
+// or one Newton-Schulz phase over every matrix of a batch).
+//   warps 0, 6  TMA producers: warp 0 loads the A half of every stage, warp
+//               6 the B half (bf16, 128-byte swizzle, K = 128 per stage in
+//               two 64-wide chunks) into a 3-stage ring
+//   warp 1      TMEM owner and MMA issuer: 8 x tcgen05.mma (K = 16) per
+//               stage, one commit per stage, into one of two fp32 TMEM
+//               accumulators
 //   warps 2..5  epilogue: tcgen05.ld -> scale / aux / RoPE -> bf16 or f32
 //               global stores (mirrored for symmetric outputs)
 // The double-buffered accumulator lets the epilogue of tile t overlap the
@@ -16,10 +18,16 @@
 
 namespace mc {
 
-constexpr int kAStageBytes = kBM * kBK * 2;  // 16 KB
-// warp 0 and warp 6: TMA producers (even and odd K blocks: one thread issues
-// TMA loads at about half the rate two threads in different warps reach);
-// warp 1: MMA issuer; warps 2..5: epilogue
+// A stage: K = kStageK in chunks of kBK (one 128-byte swizzle row each).
+// Eight MMAs per commit: a commit and the producer's wait on it cost about
+// as much as four N = 128 MMAs, so four MMAs per commit ran at half the
+// tensor rate at N = 128 (measured); eight per commit keep it near full.
+constexpr int kKChunks = kStageK / kBK;
+constexpr int kAChunkBytes = kBM * kBK * 2;            // 16 KB
+constexpr int kAStageBytes = kAChunkBytes * kKChunks;  // 32 KB
+// warp 0 and warp 6: TMA producers (the A and the B half of every stage:
+// one thread issues TMA loads at about half the rate two threads in
+// different warps reach); warp 1: MMA issuer; warps 2..5: epilogue
 constexpr int kGemmThreads = 224;
 // epilogue staging: each epilogue warp stages a 32 x 64 chunk of 16-bit
 // values in rows of 72 elements (144 B: 16-byte accesses are bank-conflict
@@ -37,7 +45,7 @@ static_assert(kEpiWarpBytes >= 32 * kStageLd * 2 && kEpiWarpBytes % 1024 == 0, "
 // layout a SWIZZLE_128B tensor map reads).
 MC_D int stage_off(bool swz, int r, int v) { return swz ? r * 64 + ((v ^ (r & 7)) << 3) : r * kStageLd + (v << 3); }
 // Tile / pipeline shapes (see the launchers at the end): CTA pairs on
-// 256 x 256 tiles, each SM holding 128 rows of A and 128 of B per 32 KB
+// 256 x 256 tiles, each SM holding 128 rows of A and 128 of B per 64 KB
 // stage; single CTAs on 128 x 128 tiles for small Newton-Schulz batches.
 // Shared-memory copies of the current and the next phase's problems: the
 // roles read the problem fields from here instead of the (large, dynamically
@@ -52,7 +60,11 @@ struct TileCfg {
     // rows (K-major) or columns (MN-major) of B; the MMA reads both halves
     static constexpr int kTileM = PAIR ? 2 * kBM : kBM;
     static constexpr int kBRows = PAIR ? BN / 2 : BN;
-    static constexpr int kBStage = kBRows * kBK * 2;
+    // K-major B: kKChunks chunks of kBRows rows x 128 bytes; MN-major B:
+    // kBRows / 64 column chunks of kStageK rows x 128 bytes
+    static constexpr int kBChunkK = kBRows * kBK * 2;
+    static constexpr int kBChunkMN = kStageK * 128;
+    static constexpr int kBStage = kBRows * kStageK * 2;
     static constexpr int kSmem = STAGES * (kAStageBytes + kBStage) + 4 * kEpiWarpBytes + 1024 + kTailBytes +
                                  64 + kProbStageBytes;
     static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
@@ -533,10 +545,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         ok = ok && !*abort_flag;
         if (warp == 0 || warp == 6) {
             // ---------------- TMA producers ----------------
-            // both walk every K block; warp 0 issues the even ones, warp 6 the
-            // odd ones (an even stage count gives each stage one producer)
-            static_assert(STAGES % 2 == 0, "stages split between two producers");
-            const int pid = warp == 6 ? 1 : 0;
+            // both walk every stage; warp 0 loads the A half (and arms the
+            // full barrier with the whole stage's bytes), warp 6 the B half.
+            // B bytes may land before the barrier is armed: the phase cannot
+            // complete before warp 0's arrival, and the transaction count
+            // only has to balance by then.
+            const bool loads_a = warp == 0;
             if (lane == 0 && ok) {
                 for (int t = t_begin + unit; t < t_end && ok; t += nunits) {
                     int pi, z, tm, tn;
@@ -544,43 +558,52 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                     const GemmProblem& q = sp[pi];
                     const CUtensorMap* tmA = &P.p[pb + pi].tmA;
                     const CUtensorMap* tmB = &P.p[pb + pi].tmB;
-                    const int nk = (q.K + kBK - 1) / kBK;
+                    const int b_mn = q.b_mn;
+                    const int nk = (q.K + kStageK - 1) / kStageK;
                     for (int kb = 0; kb < nk; ++kb) {
-                        if ((stage & 1) != pid) {  // the other producer's stage
-                            if (++stage == kGemmStages) {
-                                stage = 0;
-                                phase ^= 1;
-                            }
-                            continue;
-                        }
                         if (!mbar_wait(&tail->empty[stage], phase ^ 1, abort_flag, P.status)) {
                             ok = false;
                             break;
                         }
+                        uint8_t* a = sA + stage * kAStageBytes;
                         uint8_t* b = sB + stage * kBStageBytes;
+                        const int k0 = kb * kStageK;
                         if constexpr (PAIR) {
-                            // both halves complete on the leader's full barrier, which expects both
-                            if (leader) mbar_arrive_expect_tx(&tail->full[stage], 2 * (kAStageBytes + kBStageBytes));
+                            // both CTAs' halves complete on the leader's full barrier
                             const uint32_t fb = mapa_shared(smem_u32(&tail->full[stage]), 0);
-                            tma_load_3d_pair(sA + stage * kAStageBytes, tmA, fb, kb * kBK, tm * TM + rank * kBM, z);
-                            const int b0 = tn * BN + (int)rank * Cfg::kBRows;
-                            if (!q.b_mn) {
-                                tma_load_3d_pair(b, tmB, fb, kb * kBK, b0, z);
-                            } else {
+                            if (loads_a) {
+                                if (leader)
+                                    mbar_arrive_expect_tx(&tail->full[stage], 2 * (kAStageBytes + kBStageBytes));
 #pragma unroll
-                                for (int j = 0; j < Cfg::kBRows / 64; ++j)
-                                    tma_load_3d_pair(b + j * (kBK * 128), tmB, fb, b0 + j * 64, kb * kBK, z);
+                                for (int c = 0; c < kKChunks; ++c)
+                                    tma_load_3d_pair(a + c * kAChunkBytes, tmA, fb, k0 + c * kBK,
+                                                     tm * TM + rank * kBM, z);
+                            } else {
+                                const int b0 = tn * BN + (int)rank * Cfg::kBRows;
+                                if (!b_mn) {
+#pragma unroll
+                                    for (int c = 0; c < kKChunks; ++c)
+                                        tma_load_3d_pair(b + c * Cfg::kBChunkK, tmB, fb, k0 + c * kBK, b0, z);
+                                } else {
+#pragma unroll
+                                    for (int j = 0; j < Cfg::kBRows / 64; ++j)
+                                        tma_load_3d_pair(b + j * Cfg::kBChunkMN, tmB, fb, b0 + j * 64, k0, z);
+                                }
                             }
                         } else {
-                            mbar_arrive_expect_tx(&tail->full[stage], kAStageBytes + kBStageBytes);
-                            tma_load_3d(sA + stage * kAStageBytes, tmA, &tail->full[stage], kb * kBK, tm * kBM, z);
-                            if (!q.b_mn) {
-                                tma_load_3d(b, tmB, &tail->full[stage], kb * kBK, tn * BN, z);
+                            if (loads_a) {
+                                mbar_arrive_expect_tx(&tail->full[stage], kAStageBytes + kBStageBytes);
+#pragma unroll
+                                for (int c = 0; c < kKChunks; ++c)
+                                    tma_load_3d(a + c * kAChunkBytes, tmA, &tail->full[stage], k0 + c * kBK, tm * kBM, z);
+                            } else if (!b_mn) {
+#pragma unroll
+                                for (int c = 0; c < kKChunks; ++c)
+                                    tma_load_3d(b + c * Cfg::kBChunkK, tmB, &tail->full[stage], k0 + c * kBK, tn * BN, z);
                             } else {
 #pragma unroll
                                 for (int j = 0; j < BN / 64; ++j)
-                                    tma_load_3d(b + j * (kBK * 128), tmB, &tail->full[stage], tn * BN + j * 64,
-                                                kb * kBK, z);
+                                    tma_load_3d(b + j * Cfg::kBChunkMN, tmB, &tail->full[stage], tn * BN + j * 64, k0, z);
                             }
                         }
                         ++issued[stage];
@@ -597,8 +620,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 int pi, z, tm, tn;
                 decode_tile<BN, TM>(sp, np, t, pi, z, tm, tn);
                 const GemmProblem& q = sp[pi];
-                const int nk = (q.K + kBK - 1) / kBK;
-                const uint32_t idesc = idesc_f16kind(TM, BN, q.b_mn, q.ab_f16);
+                const int nk = (q.K + kStageK - 1) / kStageK;
+                const int b_mn = q.b_mn;
+                const uint32_t idesc = idesc_f16kind(TM, BN, b_mn, q.ab_f16);
                 if (!mbar_wait(&tail->tempty[acc], aphase ^ 1, abort_flag, P.status)) {
                     ok = false;
                     break;
@@ -612,13 +636,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                     }
                     tc_fence_after();
                     if (lane == 0) {
-                        const uint32_t a0 = smem_u32(sA + stage * kAStageBytes);
-                        const uint32_t b0 = smem_u32(sB + stage * kBStageBytes);
+                        // stage descriptors once; a K step moves the 16-byte
+                        // address field: +32 B within a K-major chunk, +16 KB
+                        // (A) or one B chunk to the next chunk, +2 KB per
+                        // step down an MN-major chunk
+                        const uint64_t a_d = sw128_desc(smem_u32(sA + stage * kAStageBytes), 16, 1024);
+                        const uint64_t b_d = b_mn ? sw128_desc(smem_u32(sB + stage * kBStageBytes), Cfg::kBChunkMN, 1024)
+                                                  : sw128_desc(smem_u32(sB + stage * kBStageBytes), 16, 1024);
 #pragma unroll
-                        for (int k = 0; k < kBK / 16; ++k) {
-                            uint64_t ad = sw128_desc(a0 + k * 32, 16, 1024);
-                            uint64_t bd = q.b_mn ? sw128_desc(b0 + k * 2048, kBK * 128, 1024)
-                                                 : sw128_desc(b0 + k * 32, 16, 1024);
+                        for (int k = 0; k < kStageK / 16; ++k) {
+                            const uint64_t ad = a_d + (uint64_t)((k >> 2) * (kAChunkBytes >> 4) + (k & 3) * 2);
+                            const uint64_t bd = b_mn ? b_d + (uint64_t)(k * (2048 >> 4))
+                                                     : b_d + (uint64_t)((k >> 2) * (Cfg::kBChunkK >> 4) + (k & 3) * 2);
                             if constexpr (PAIR)
                                 umma_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
                             else
@@ -802,20 +831,20 @@ static cudaError_t launch_cfg(const GemmParamsT<MAXP>& P, bool coop, cudaStream_
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-// Configurations: 256 x 256 tiles on CTA pairs with 6 stages of 32 KB per
+// Configurations: 256 x 256 tiles on CTA pairs with 3 stages of 64 KB per
 // SM (projections, plain GEMMs, large Newton-Schulz batches); 128 x 128
-// tiles on single CTAs with 6 stages of 32 KB (small Newton-Schulz batches).
+// tiles on single CTAs with 3 stages of 64 KB (small Newton-Schulz batches).
 cudaError_t launch_gemm(const GemmParams& P, cudaStream_t stream, const char* label) {
     if (P.total_tiles <= 0) return cudaSuccess;
     if (!phases_fit(P)) return cudaErrorInvalidValue;
-    return launch_cfg<kMaxProblems, kBN, 6, true>(P, false, stream, label);
+    return launch_cfg<kMaxProblems, kBN, 3, true>(P, false, stream, label);
 }
 
 cudaError_t launch_gemm_multi(const GemmParamsMulti& P, cudaStream_t stream, const char* label) {
     if (P.total_tiles <= 0) return cudaSuccess;
     if (!phases_fit(P)) return cudaErrorInvalidValue;
-    if (P.tile_m == 2 * kBM) return launch_cfg<kMaxProblemsMulti, kBN, 6, true>(P, true, stream, label);
-    return launch_cfg<kMaxProblemsMulti, 128, 6, false>(P, true, stream, label);
+    if (P.tile_m == 2 * kBM) return launch_cfg<kMaxProblemsMulti, kBN, 3, true>(P, true, stream, label);
+    return launch_cfg<kMaxProblemsMulti, 128, 3, false>(P, true, stream, label);
 }
 
 }  // namespace mc

@@ -18,7 +18,8 @@ namespace mc {
 // ---------------------------------------------------------------------------
 constexpr int kBM = 128;  // UMMA M (TMEM lanes)
 constexpr int kBN = 256;  // UMMA N (TMEM columns per accumulator)
-constexpr int kBK = 64;   // K per smem stage: one 128-byte swizzle row of bf16
+constexpr int kBK = 64;   // K of one 128-byte swizzle row of bf16: one TMA box, one descriptor chunk
+constexpr int kStageK = 128;  // K per pipeline stage: two such chunks, 8 MMAs (K = 16) per commit
 constexpr int kMaxProblems = 4;        // problems of a single-phase launch
 constexpr int kMaxProblemsMulti = 48;  // problems of a multi-phase launch (kernel parameters < 32 KB)
 constexpr int kMaxPhases = 16;
@@ -35,7 +36,7 @@ constexpr int kOutBF16 = 0, kOutF32 = 1, kOutF16 = 2;
 
 struct GemmProblem {
     CUtensorMap tmA;  // 3D {K, M, batch}, box {64, 128}, 128B swizzle
-    CUtensorMap tmB;  // K-major {K, N, batch} box {64, 256}; MN-major {N, K, batch} box {64, 64}
+    CUtensorMap tmB;  // K-major {K, N, batch} box {64, rows}; MN-major {N, K, batch} box {64, 128}
     CUtensorMap tmC;  // bulk_st: the 16-bit output {N, M, batch}, box {64, 32}, 128B swizzle
     int M, N, K, batch;
     int b_mn, sym, out_kind, vec_ok;  // out_kind: kOutBF16 / kOutF32 / kOutF16
