@@ -25,17 +25,29 @@
 
 namespace mc {
 
-constexpr int kAttnThreads = 192;
-constexpr int kAttnBlk = 128;          // queries per item, keys per key block
+// 384 threads, three warpgroups:
+//   warpgroup 0  warp 0: TMA of Q (both tiles) and K; warp 1: TMEM owner and
+//                MMA issuer; warp 2: TMA of V; warp 3 idle
+//   warpgroup 1  softmax and output of query tile 0 (one row per thread)
+//   warpgroup 2  softmax and output of query tile 1
+// Registers move from warpgroup 0 to the softmax warpgroups with setmaxnreg
+// (128 x 88 + 256 x 200 = 62464 <= 384 threads x 168 at launch); each
+// warpgroup's branch starts with its setmaxnreg, so the compiler allocates
+// the softmax code with 200 registers (128 logits per thread stay in them).
+constexpr int kAttnThreads = 384;
+constexpr int kAttnRegsLow = 88, kAttnRegsHigh = 200;
+static_assert(128 * kAttnRegsLow + 256 * kAttnRegsHigh <= kAttnThreads * (65536 / kAttnThreads / 8 * 8),
+              "register split");
+constexpr int kAttnBlk = 128;          // queries per tile, keys per key block
 constexpr int kAttnMaxStages = 4;
 constexpr int kAttnTile = 16384;       // 128 rows x 64 bf16 (one 128-byte-swizzled block)
-constexpr int kAttnRing = 224 * 1024;  // Q + two P tiles + K/V stages
+constexpr int kAttnRing = 224 * 1024;  // Q and P of two tiles, then the K and V rings
 constexpr int kAttnSmem = 1024 + 1024 + kAttnRing;
 
 struct AttnParams {
     CUtensorMap tmQ, tmK, tmV;  // {H*dh, T, B} bf16, box {64, 128}
     int B, T, H, dh, causal;
-    int n_it, total_items, band, stages;
+    int n_it, n_pair, total_items, band, kst, vst;
     __nv_bfloat16* o;
     long long ld;               // H * dh: row stride of q, k, v and o
     float scale_log2;           // log2(e) / sqrt(dh)
@@ -49,12 +61,13 @@ struct AttnParams {
 };
 
 struct AttnSmemTail {
-    uint64_t kvfull[kAttnMaxStages], kvempty[kAttnMaxStages];
+    uint64_t kfull[kAttnMaxStages], kempty[kAttnMaxStages];
+    uint64_t vfull[kAttnMaxStages], vempty[kAttnMaxStages];
     uint64_t qfull, qempty;
-    uint64_t sfull[2], sempty[2];
+    uint64_t sfull[2], sempty[2];  // per query tile
     uint64_t pfull[2];
-    uint64_t oready;  // one phase per P.V product
-    uint64_t oempty;  // the item's output has been read from TMEM
+    uint64_t oready[2];  // one phase per P.V product of the tile
+    uint64_t oempty[2];  // the tile's output of an item has been read from TMEM
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -69,19 +82,27 @@ MC_D float ex2_approx(float x) {
     return y;
 }
 
-MC_D void attn_item(const AttnParams& P, int i, int& b, int& h, int& it, int& njb) {
+// Item i -> (b, h, tile pair g) and the key blocks of its two query tiles
+// 2g and 2g + 1 (0 when the tile lies past the sequence).
+MC_D void attn_item(const AttnParams& P, int i, int& b, int& h, int& g, int (&njb)[2]) {
     const int BH = P.B * P.H;
-    const int per_band = P.band * P.n_it;
+    const int per_band = P.band * P.n_pair;
     const int band = i / per_band;
     const int w = i - band * per_band;
     const int pairs = min(P.band, BH - band * P.band);
     const int grp = w / pairs;
     const int bh = band * P.band + (w - grp * pairs);
-    it = P.causal ? (P.n_it - 1 - grp) : grp;  // heaviest causal tiles first
+    g = P.causal ? (P.n_pair - 1 - grp) : grp;  // heaviest causal pairs first
     b = bh / P.H;
     h = bh - b * P.H;
-    const int row_end = min(P.T, (it + 1) * kAttnBlk);
-    njb = P.causal ? (row_end - 1) / kAttnBlk + 1 : (P.T + kAttnBlk - 1) / kAttnBlk;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int it = 2 * g + t;
+        const int row_end = min(P.T, (it + 1) * kAttnBlk);
+        njb[t] = it >= P.n_it ? 0
+                 : P.causal   ? (row_end - 1) / kAttnBlk + 1
+                              : (P.T + kAttnBlk - 1) / kAttnBlk;
+    }
 }
 
 MC_D int attn_round_item(int r) {
@@ -89,35 +110,42 @@ MC_D int attn_round_item(int r) {
     return r * (int)gridDim.x + c;
 }
 
+template <uint32_t N>
+MC_D void setmaxnreg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+template <uint32_t N>
+MC_D void setmaxnreg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
+
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_constant__ AttnParams P) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     static_assert(sizeof(AttnSmemTail) <= 1024, "tail");
     AttnSmemTail* tail = reinterpret_cast<AttnSmemTail*>(smem);
     const int nc = P.dh / 64;                 // 64-column blocks per row of q, k, v
-    const int nst = P.stages;
-    uint8_t* sQ = smem + 1024;                // nc blocks
-    uint8_t* sP = sQ + nc * kAttnTile;        // two P tiles of 2 blocks (128 keys)
-    uint8_t* sKV = sP + 4 * kAttnTile;        // stage s: K at sKV + s * 2nc blocks, V after it
+    uint8_t* sQ = smem + 1024;                // tile t: blocks t*nc ..
+    uint8_t* sP = sQ + 2 * nc * kAttnTile;    // tile t: 2 blocks (128 keys) at sP + 2t blocks
+    uint8_t* sK = sP + 4 * kAttnTile;         // stage s: nc blocks
+    uint8_t* sV = sK + P.kst * nc * kAttnTile;
     volatile int* abort_flag = &tail->abort_flag;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t kv_bytes = (uint32_t)(2 * nc * kAttnTile);
+    const uint32_t blk_bytes = (uint32_t)(nc * kAttnTile);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < nst; ++s) {
-            mbar_init(&tail->kvfull[s], 1);
-            mbar_init(&tail->kvempty[s], 1);
+        for (int s = 0; s < kAttnMaxStages; ++s) {
+            mbar_init(&tail->kfull[s], 1);
+            mbar_init(&tail->kempty[s], 1);
+            mbar_init(&tail->vfull[s], 1);
+            mbar_init(&tail->vempty[s], 1);
         }
         mbar_init(&tail->qfull, 1);
         mbar_init(&tail->qempty, 1);
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(&tail->sfull[a], 1);
-            mbar_init(&tail->sempty[a], 4);
-            mbar_init(&tail->pfull[a], 4);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&tail->sfull[t], 1);
+            mbar_init(&tail->sempty[t], 4);
+            mbar_init(&tail->pfull[t], 4);
+            mbar_init(&tail->oready[t], 1);
+            mbar_init(&tail->oempty[t], 4);
         }
-        mbar_init(&tail->oready, 1);
-        mbar_init(&tail->oempty, 4);
         mbar_init(&tail->drain, 1);
         tail->abort_flag = 0;
         fence_mbar_init();
@@ -134,38 +162,47 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem_base = tail->tmem_base;
-    const uint32_t tO = tmem_base + 256;      // S tiles at columns 0 and 128, O after them
+    const uint32_t tmem_base = tail->tmem_base;  // S tiles at columns 0 and 128, O tiles from 256
     pdl_wait();
 
-    if (warp == 0) {
-        // ---------------- TMA producer ----------------
+    if (warp < 4) {
+    setmaxnreg_dec<kAttnRegsLow>();
+    if (warp == 0 || warp == 2) {
+        // ---------------- TMA producers: Q and K (warp 0), V (warp 2) ----------------
         if (lane == 0) {
+            const bool is_k = warp == 0;
+            const int nst = is_k ? P.kst : P.vst;
+            uint64_t* full = is_k ? tail->kfull : tail->vfull;
+            uint64_t* empty = is_k ? tail->kempty : tail->vempty;
+            uint8_t* ring = is_k ? sK : sV;
+            const CUtensorMap* tm = is_k ? &P.tmK : &P.tmV;
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued[kAttnMaxStages] = {0, 0, 0, 0};
             uint32_t n = 0;
             bool ok = true;
             for (int r = 0, i = attn_round_item(0); i < P.total_items && ok; i = attn_round_item(++r), ++n) {
-                int b, h, it, njb;
-                attn_item(P, i, b, h, it, njb);
-                if (!mbar_wait(&tail->qempty, (n & 1) ^ 1, abort_flag, P.status)) break;
-                mbar_arrive_expect_tx(&tail->qfull, (uint32_t)(nc * kAttnTile));
-                for (int c = 0; c < nc; ++c)
-                    tma_load_3d(sQ + c * kAttnTile, &P.tmQ, &tail->qfull, h * P.dh + c * 64, it * kAttnBlk, b);
-                for (int j = 0; j < njb; ++j) {
-                    if (!mbar_wait(&tail->kvempty[stage], phase ^ 1, abort_flag, P.status)) {
+                int b, h, g, njb[2];
+                attn_item(P, i, b, h, g, njb);
+                if (is_k) {
+                    // both Q tiles (the second may lie past the sequence: zeros)
+                    if (!mbar_wait(&tail->qempty, (n & 1) ^ 1, abort_flag, P.status)) break;
+                    mbar_arrive_expect_tx(&tail->qfull, 2 * blk_bytes);
+                    for (int t = 0; t < 2; ++t)
+                        for (int c = 0; c < nc; ++c)
+                            tma_load_3d(sQ + (t * nc + c) * kAttnTile, &P.tmQ, &tail->qfull, h * P.dh + c * 64,
+                                        (2 * g + t) * kAttnBlk, b);
+                }
+                const int nj = max(njb[0], njb[1]);
+                for (int j = 0; j < nj; ++j) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, P.status)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&tail->kvfull[stage], kv_bytes);
-                    uint8_t* sk = sKV + stage * 2 * nc * kAttnTile;
-                    for (int c = 0; c < nc; ++c) {
-                        tma_load_3d(sk + c * kAttnTile, &P.tmK, &tail->kvfull[stage], h * P.dh + c * 64,
+                    mbar_arrive_expect_tx(&full[stage], blk_bytes);
+                    for (int c = 0; c < nc; ++c)
+                        tma_load_3d(ring + (stage * nc + c) * kAttnTile, tm, &full[stage], h * P.dh + c * 64,
                                     j * kAttnBlk, b);
-                        tma_load_3d(sk + (nc + c) * kAttnTile, &P.tmV, &tail->kvfull[stage], h * P.dh + c * 64,
-                                    j * kAttnBlk, b);
-                    }
                     ++issued[stage];
                     if (++stage == nst) {
                         stage = 0;
@@ -176,114 +213,142 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
             // the copies still in flight land before exit
             volatile int never = 0;
             for (int s = 0; s < nst; ++s)
-                if (issued[s]) mbar_wait(&tail->kvfull[s], (issued[s] - 1) & 1, &never, P.status);
-            if (n) mbar_wait(&tail->qfull, (n - 1) & 1, &never, P.status);
+                if (issued[s]) mbar_wait(&full[s], (issued[s] - 1) & 1, &never, P.status);
+            if (is_k && n) mbar_wait(&tail->qfull, (n - 1) & 1, &never, P.status);
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         const uint32_t idesc_s = idesc_f16kind(kAttnBlk, kAttnBlk, 0, 0);  // S = Q K^T, K-major K
         const uint32_t idesc_o = idesc_f16kind(kAttnBlk, P.dh, 1, 0);      // O += P V, MN-major V
-        int stage = 0;
-        uint32_t phase = 0;
-        uint32_t sc = 0, pc = 0, n = 0;  // S tiles, P.V products, items
+        int ks = 0, vs = 0;
+        uint32_t kph = 0, vph = 0;
+        uint32_t sc[2] = {0, 0}, pc[2] = {0, 0}, no[2] = {0, 0}, n = 0;
         bool ok = true;
-        // O += P_j V_j for the block in ring stage st; the first of an item
-        // overwrites O once the previous item's output has been read
-        auto pv = [&](int j, int st) {
-            if (j == 0 && !mbar_wait(&tail->oempty, (n & 1) ^ 1, abort_flag, P.status)) return false;
-            if (!mbar_wait(&tail->pfull[pc & 1], (pc >> 1) & 1, abort_flag, P.status)) return false;
-            tc_fence_after();
-            if (lane == 0) {
-                const uint32_t p0 = smem_u32(sP + (pc & 1) * 2 * kAttnTile);
-                const uint32_t v0 = smem_u32(sKV + st * 2 * nc * kAttnTile + nc * kAttnTile);
+        int njb[2];
+        // O_t += P_t V_jj for both tiles that use key block jj; the first
+        // product of an item overwrites O_t once the previous output is read
+        auto pv = [&](int jj) {
+            if (!mbar_wait(&tail->vfull[vs], vph, abort_flag, P.status)) return false;
+            for (int t = 0; t < 2; ++t) {
+                if (jj >= njb[t]) continue;
+                if (jj == 0 && !mbar_wait(&tail->oempty[t], (no[t] & 1) ^ 1, abort_flag, P.status)) return false;
+                if (!mbar_wait(&tail->pfull[t], pc[t] & 1, abort_flag, P.status)) return false;
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t p0 = smem_u32(sP + 2 * t * kAttnTile);
+                    const uint32_t v0 = smem_u32(sV + vs * nc * kAttnTile);
+                    const uint32_t tO = tmem_base + 256 + t * P.dh;
 #pragma unroll
-                for (int k = 0; k < kAttnBlk / 16; ++k) {
-                    const uint64_t ad = sw128_desc(p0 + (k >> 2) * kAttnTile + (k & 3) * 32, 16, 1024);
-                    const uint64_t bd = sw128_desc(v0 + k * 2048, kAttnTile, 1024);
-                    umma_bf16(tO, ad, bd, idesc_o, (j | k) != 0);
+                    for (int k = 0; k < kAttnBlk / 16; ++k) {
+                        const uint64_t ad = sw128_desc(p0 + (k >> 2) * kAttnTile + (k & 3) * 32, 16, 1024);
+                        const uint64_t bd = sw128_desc(v0 + k * 2048, kAttnTile, 1024);
+                        umma_bf16(tO, ad, bd, idesc_o, (jj | k) != 0);
+                    }
+                    umma_commit(&tail->oready[t]);
                 }
-                umma_commit(&tail->oready);
-                umma_commit(&tail->kvempty[st]);  // K_j and V_j are both consumed now
+                __syncwarp();
+                ++pc[t];
+                if (jj == njb[t] - 1) ++no[t];
             }
+            if (lane == 0) umma_commit(&tail->vempty[vs]);  // V_jj consumed by both tiles
             __syncwarp();
-            ++pc;
+            if (++vs == P.vst) {
+                vs = 0;
+                vph ^= 1;
+            }
             return true;
         };
         for (int r = 0, i = attn_round_item(0); i < P.total_items && ok; i = attn_round_item(++r), ++n) {
-            int b, h, it, njb;
-            attn_item(P, i, b, h, it, njb);
+            int b, h, g;
+            attn_item(P, i, b, h, g, njb);
+            const int nj = max(njb[0], njb[1]);
             if (!mbar_wait(&tail->qfull, n & 1, abort_flag, P.status)) break;
-            tc_fence_after();
-            const uint32_t q0 = smem_u32(sQ);
-            int prev_stage = -1;
-            for (int j = 0; j < njb && ok; ++j) {
-                // S_j = Q K_j^T
-                if (!mbar_wait(&tail->kvfull[stage], phase, abort_flag, P.status) ||
-                    !mbar_wait(&tail->sempty[sc & 1], ((sc >> 1) & 1) ^ 1, abort_flag, P.status)) {
+            for (int j = 0; j < nj && ok; ++j) {
+                // S_t = Q_t K_j^T for the tiles that use key block j
+                if (!mbar_wait(&tail->kfull[ks], kph, abort_flag, P.status)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t k0 = smem_u32(sKV + stage * 2 * nc * kAttnTile);
-                    const uint32_t ts = tmem_base + (sc & 1) * kAttnBlk;
-                    for (int k = 0; k < P.dh / 16; ++k) {
-                        const uint32_t off = (k >> 2) * kAttnTile + (k & 3) * 32;
-                        umma_bf16(ts, sw128_desc(q0 + off, 16, 1024), sw128_desc(k0 + off, 16, 1024), idesc_s,
-                                  k != 0);
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (j >= njb[t]) continue;
+                    if (!mbar_wait(&tail->sempty[t], (sc[t] & 1) ^ 1, abort_flag, P.status)) {
+                        ok = false;
+                        break;
                     }
-                    umma_commit(&tail->sfull[sc & 1]);
-                    if (j == njb - 1) umma_commit(&tail->qempty);  // the item's last use of Q
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t q0 = smem_u32(sQ + t * nc * kAttnTile);
+                        const uint32_t k0 = smem_u32(sK + ks * nc * kAttnTile);
+                        const uint32_t ts = tmem_base + t * kAttnBlk;
+                        for (int k = 0; k < P.dh / 16; ++k) {
+                            const uint32_t off = (k >> 2) * kAttnTile + (k & 3) * 32;
+                            umma_bf16(ts, sw128_desc(q0 + off, 16, 1024), sw128_desc(k0 + off, 16, 1024), idesc_s,
+                                      k != 0);
+                        }
+                        umma_commit(&tail->sfull[t]);
+                    }
+                    __syncwarp();
+                    ++sc[t];
+                }
+                if (!ok) break;
+                if (lane == 0) {
+                    umma_commit(&tail->kempty[ks]);                // K_j consumed
+                    if (j == nj - 1) umma_commit(&tail->qempty);  // the item's last use of Q
                 }
                 __syncwarp();
-                ++sc;
-                const int cur = stage;
-                if (++stage == nst) {
-                    stage = 0;
-                    phase ^= 1;
+                if (++ks == P.kst) {
+                    ks = 0;
+                    kph ^= 1;
                 }
-                // O += P_{j-1} V_{j-1} while the softmax works on S_j
-                if (j >= 1 && !pv(j - 1, prev_stage)) {
+                // O_t += P_t V_{j-1} while the softmax works on S_j
+                if (j >= 1 && !pv(j - 1)) {
                     ok = false;
                     break;
                 }
-                prev_stage = cur;
             }
             if (!ok) break;
-            if (!pv(njb - 1, prev_stage)) break;
+            if (!pv(nj - 1)) break;
         }
         if (lane == 0) umma_commit(&tail->drain);
         __syncwarp();
         volatile int never = 0;
         mbar_wait(&tail->drain, 0, &never, P.status);
+    }
     } else {
-        // ---------------- softmax and output (warps 2..5) ----------------
-        const int quarter = warp & 3;  // TMEM lanes 32 q .. 32 q + 31
-        const int lr = quarter * 32 + lane;  // row of the item's tile
+        setmaxnreg_inc<kAttnRegsHigh>();
+        // ---------------- softmax and output: tile t = warpgroup - 1 ----------------
+        const int t = warp >= 8 ? 1 : 0;
+        const int quarter = warp & 3;        // TMEM lanes 32 q .. 32 q + 31
+        const int lr = quarter * 32 + lane;  // row of the tile
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        uint32_t sc = 0, pc = 0, n = 0;
+        const uint32_t tS = tmem_base + lane_base + t * kAttnBlk;
+        const uint32_t tO = tmem_base + lane_base + 256 + t * P.dh;
+        uint8_t* pt = sP + 2 * t * kAttnTile;
+        uint32_t sc = 0, pc = 0;
         bool ok = true;
-        for (int r = 0, i = attn_round_item(0); i < P.total_items && ok; i = attn_round_item(++r), ++n) {
-            int b, h, it, njb;
-            attn_item(P, i, b, h, it, njb);
+        for (int r = 0, i = attn_round_item(0); i < P.total_items && ok; i = attn_round_item(++r)) {
+            int b, h, g, njb[2];
+            attn_item(P, i, b, h, g, njb);
+            const int nj = njb[t];
+            if (nj == 0) continue;  // the tile lies past the sequence
+            const int it = 2 * g + t;
             const int row = it * kAttnBlk + lr;
             const bool row_ok = row < P.T;
             float m = -INFINITY, l = 0.f, m_raw = -INFINITY;
-            for (int j = 0; j < njb && ok; ++j) {
-                if (!mbar_wait(&tail->sfull[sc & 1], (sc >> 1) & 1, abort_flag, P.status)) {
+            for (int j = 0; j < nj && ok; ++j) {
+                if (!mbar_wait(&tail->sfull[t], sc & 1, abort_flag, P.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 float v[kAttnBlk];
                 uint32_t* vu = reinterpret_cast<uint32_t*>(v);
-                const uint32_t ts = tmem_base + lane_base + (sc & 1) * kAttnBlk;
 #pragma unroll
-                for (int c = 0; c < kAttnBlk / 32; ++c) tmem_ld32(ts + c * 32, vu + c * 32);
+                for (int c = 0; c < kAttnBlk / 32; ++c) tmem_ld32(tS + c * 32, vu + c * 32);
                 tmem_ld_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&tail->sempty[sc & 1]);
+                if (lane == 0) mbar_arrive(&tail->sempty[t]);
                 ++sc;
                 // mask (keys past T; keys after the row when causal; rows past T)
                 const int key0 = j * kAttnBlk;
@@ -321,8 +386,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                 l = __fmaf_rn(l, alpha, lsum);
                 m = m_new;
                 if (j >= 1) {
-                    // O and P tile (pc & 1) are free once P_{j-1} V_{j-1} is done
-                    if (!mbar_wait(&tail->oready, (pc - 1) & 1, abort_flag, P.status)) {
+                    // O_t and the P tile are free once P_{j-1} V_{j-1} is done
+                    if (!mbar_wait(&tail->oready[t], (pc - 1) & 1, abort_flag, P.status)) {
                         ok = false;
                         break;
                     }
@@ -330,17 +395,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                     if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
                         for (int c = 0; c < P.dh / 32; ++c) {
                             uint32_t o[32];
-                            tmem_ld32(tO + lane_base + c * 32, o);
+                            tmem_ld32(tO + c * 32, o);
                             tmem_ld_wait();
 #pragma unroll
                             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                            tmem_st32(tO + lane_base + c * 32, o);
+                            tmem_st32(tO + c * 32, o);
                         }
                         tmem_st_wait();
                     }
                 }
                 // P_j as bf16, 128-byte swizzled K-major rows (two 64-key blocks)
-                uint8_t* pt = sP + (pc & 1) * 2 * kAttnTile;
 #pragma unroll
                 for (int cc = 0; cc < kAttnBlk / 8; ++cc) {
                     __nv_bfloat162 hh[4];
@@ -352,18 +416,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                 fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&tail->pfull[pc & 1]);
+                if (lane == 0) mbar_arrive(&tail->pfull[t]);
                 ++pc;
             }
             if (!ok) break;
-            // the item's output: O / l once the last P.V product is done
-            if (!mbar_wait(&tail->oready, (pc - 1) & 1, abort_flag, P.status)) break;
+            // the tile's output: O / l once its last P.V product is done
+            if (!mbar_wait(&tail->oready[t], (pc - 1) & 1, abort_flag, P.status)) break;
             tc_fence_after();
             const float inv = row_ok ? 1.f / l : 0.f;
             __nv_bfloat16* orow = P.o + ((size_t)b * P.T + (row_ok ? row : 0)) * P.ld + (size_t)h * P.dh;
             for (int c = 0; c < P.dh / 32; ++c) {
                 uint32_t o[32];
-                tmem_ld32(tO + lane_base + c * 32, o);
+                tmem_ld32(tO + c * 32, o);
                 tmem_ld_wait();
                 if (row_ok) {
 #pragma unroll
@@ -379,7 +443,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&tail->oempty);
+            if (lane == 0) mbar_arrive(&tail->oempty[t]);
             // S_max: the raw max of the rows inside the sequence
             const float mw = warp_max_nan(row_ok ? m_raw : -INFINITY);
             if (lane == 0 && mw != -INFINITY) atomicMax(&P.keys[b * P.H + h], float_key(mw));
@@ -419,7 +483,8 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {
     P.dh = a.dh;
     P.causal = a.causal;
     P.n_it = (a.T + kAttnBlk - 1) / kAttnBlk;
-    P.total_items = a.B * a.H * P.n_it;
+    P.n_pair = (P.n_it + 1) / 2;
+    P.total_items = a.B * a.H * P.n_pair;
     P.o = reinterpret_cast<__nv_bfloat16*>(a.o);
     P.ld = (long long)ld;
     P.scale_log2 = (float)(1.4426950408889634 / sqrt((double)a.dh));
@@ -430,9 +495,13 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {
     P.s_max = a.s_max;
     P.s_bh = a.s_bh;
     P.status = device_status_ptr();
+    // after Q and P of two tiles: K and V rings of nc-block stages (4 + 4 at
+    // dh = 64; 2 + 1 at dh = 128, where V is needed a softmax later than K)
     const int nc = a.dh / 64;
-    // stages of K + V tiles after Q and two P tiles (4 at dh = 64, 2 at 128)
-    P.stages = std::min(kAttnMaxStages, (kAttnRing - (nc + 4) * kAttnTile) / (2 * nc * kAttnTile));
+    const int room = kAttnRing / kAttnTile - 2 * nc - 4;  // in 16 KB blocks
+    P.kst = nc == 1 ? 4 : 2;
+    P.vst = nc == 1 ? 4 : 1;
+    if ((P.kst + P.vst) * nc > room) return cudaErrorInvalidValue;
     static bool attr_set[64] = {false};
     int dev = current_device();
     if (dev < 0) return cudaErrorInvalidDevice;
@@ -443,7 +512,7 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {
     }
     int grid = num_sms();
     if (grid > P.total_items) grid = P.total_items;
-    P.band = std::max(1, std::min(a.B * a.H, (2 * grid + P.n_it - 1) / P.n_it));
+    P.band = std::max(1, std::min(a.B * a.H, (2 * grid + P.n_pair - 1) / P.n_pair));
     TraceScope ts("attn", stream);
     return launch_pdl(attn_kernel, dim3(grid), dim3(kAttnThreads), kAttnSmem, stream, P);
 }
