@@ -31,11 +31,11 @@ namespace mc {
 //   warpgroup 1  softmax and output of query tile 0 (one row per thread)
 //   warpgroup 2  softmax and output of query tile 1
 // Registers move from warpgroup 0 to the softmax warpgroups with setmaxnreg
-// (128 x 88 + 256 x 200 = 62464 <= 384 threads x 168 at launch); each
+// (128 x 120 + 256 x 184 = 62464 <= 384 threads x 168 at launch); each
 // warpgroup's branch starts with its setmaxnreg, so the compiler allocates
-// the softmax code with 200 registers (128 logits per thread stay in them).
+// the softmax code with 184 registers (128 logits per thread stay in them).
 constexpr int kAttnThreads = 384;
-constexpr int kAttnRegsLow = 88, kAttnRegsHigh = 200;
+constexpr int kAttnRegsLow = 120, kAttnRegsHigh = 184;
 static_assert(128 * kAttnRegsLow + 256 * kAttnRegsHigh <= kAttnThreads * (65536 / kAttnThreads / 8 * 8),
               "register split");
 constexpr int kAttnBlk = 128;          // queries per tile, keys per key block
@@ -108,6 +108,27 @@ MC_D void attn_item(const AttnParams& P, int i, int& b, int& h, int& g, int (&nj
 MC_D int attn_round_item(int r) {
     const int c = (r & 1) ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
     return r * (int)gridDim.x + c;
+}
+
+// The MMA warp shares its SM sub-partition with two softmax warps, so its
+// issue path is kept short: descriptors are formed once per tile or stage
+// and a K step only adds a constant to the 16-byte address field.
+// S_t = Q_t K^T: K-major Q and K, nc 64-wide blocks of 4 steps each.
+template <int NC>
+MC_D void issue_s(uint32_t d_tmem, uint64_t qd, uint64_t kd, uint32_t idesc) {
+#pragma unroll
+    for (int k = 0; k < 4 * NC; ++k) {
+        const uint64_t off = (uint64_t)(((k >> 2) * kAttnTile + (k & 3) * 32) >> 4);
+        umma_bf16(d_tmem, qd + off, kd + off, idesc, k != 0);
+    }
+}
+// O_t (+)= P_t V: P K-major (two 64-key blocks), V MN-major (2 KB per K step)
+MC_D void issue_pv(uint32_t d_tmem, uint64_t pd, uint64_t vd, uint32_t idesc, bool acc) {
+#pragma unroll
+    for (int k = 0; k < kAttnBlk / 16; ++k) {
+        const uint64_t aoff = (uint64_t)(((k >> 2) * kAttnTile + (k & 3) * 32) >> 4);
+        umma_bf16(d_tmem, pd + aoff, vd + (uint64_t)(k * (2048 >> 4)), idesc, acc || k != 0);
+    }
 }
 
 template <uint32_t N>
@@ -225,6 +246,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         uint32_t sc[2] = {0, 0}, pc[2] = {0, 0}, no[2] = {0, 0}, n = 0;
         bool ok = true;
         int njb[2];
+        // descriptors of tile 0 / ring stage 0; tile 1 and stage s add a
+        // multiple of the block size (in 16-byte units) to the address field
+        const uint64_t qdesc0 = sw128_desc(smem_u32(sQ), 16, 1024);
+        const uint64_t pdesc0 = sw128_desc(smem_u32(sP), 16, 1024);
+        const uint64_t kdesc0 = sw128_desc(smem_u32(sK), 16, 1024);
+        const uint64_t vdesc0 = sw128_desc(smem_u32(sV), kAttnTile, 1024);
+        const uint64_t blk16 = (uint64_t)(nc * kAttnTile) >> 4;  // one stage or one Q tile
         // O_t += P_t V_jj for both tiles that use key block jj; the first
         // product of an item overwrites O_t once the previous output is read
         auto pv = [&](int jj) {
@@ -235,15 +263,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                 if (!mbar_wait(&tail->pfull[t], pc[t] & 1, abort_flag, P.status)) return false;
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t p0 = smem_u32(sP + 2 * t * kAttnTile);
-                    const uint32_t v0 = smem_u32(sV + vs * nc * kAttnTile);
-                    const uint32_t tO = tmem_base + 256 + t * P.dh;
-#pragma unroll
-                    for (int k = 0; k < kAttnBlk / 16; ++k) {
-                        const uint64_t ad = sw128_desc(p0 + (k >> 2) * kAttnTile + (k & 3) * 32, 16, 1024);
-                        const uint64_t bd = sw128_desc(v0 + k * 2048, kAttnTile, 1024);
-                        umma_bf16(tO, ad, bd, idesc_o, (jj | k) != 0);
-                    }
+                    issue_pv(tmem_base + 256 + t * P.dh, pdesc0 + (uint64_t)(t * ((2 * kAttnTile) >> 4)),
+                             vdesc0 + (uint64_t)vs * blk16, idesc_o, jj != 0);
                     umma_commit(&tail->oready[t]);
                 }
                 __syncwarp();
@@ -277,14 +298,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                     }
                     tc_fence_after();
                     if (lane == 0) {
-                        const uint32_t q0 = smem_u32(sQ + t * nc * kAttnTile);
-                        const uint32_t k0 = smem_u32(sK + ks * nc * kAttnTile);
-                        const uint32_t ts = tmem_base + t * kAttnBlk;
-                        for (int k = 0; k < P.dh / 16; ++k) {
-                            const uint32_t off = (k >> 2) * kAttnTile + (k & 3) * 32;
-                            umma_bf16(ts, sw128_desc(q0 + off, 16, 1024), sw128_desc(k0 + off, 16, 1024), idesc_s,
-                                      k != 0);
-                        }
+                        const uint64_t qd = qdesc0 + (uint64_t)t * blk16, kd = kdesc0 + (uint64_t)ks * blk16;
+                        if (nc == 1)
+                            issue_s<1>(tmem_base + t * kAttnBlk, qd, kd, idesc_s);
+                        else
+                            issue_s<2>(tmem_base + t * kAttnBlk, qd, kd, idesc_s);
                         umma_commit(&tail->sfull[t]);
                     }
                     __syncwarp();
