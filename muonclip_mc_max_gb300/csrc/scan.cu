@@ -11,7 +11,8 @@
 // Work item = (sequence b, head h, 128-query tile).  One persistent CTA per
 // SM; items are dealt round-robin, heaviest causal rows first.
 //   warp 0      TMA: the item's Q tile (128 x d, d/64 blocks) once, then the
-//               K tiles (256 keys x 64) of every key tile into a 4-stage ring
+//               K tiles (256 keys x 64) of every key tile into a ring of up to
+//               6 stages
 //   warp 1      tcgen05.mma Q K^T into one of two 128 x 256 fp32 TMEM tiles
 //   warps 2..5  tcgen05.ld -> running row max (max.NaN, 4 chains) with the
 //               causal / sequence-end mask only on edge tiles; at the end of
