@@ -659,7 +659,7 @@ def run_ours(args, wl):
         line = {
             "metric": getattr(wl, "metric", METRIC), "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16/fp16",
             "data": "synthetic",
             "config": {"workload": wl.desc, "l2": "flushed between timed steps (256 MiB write)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},

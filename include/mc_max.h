@@ -246,10 +246,13 @@ size_t mc_muon_workspace_size(const int* rows, const int* cols, int count);
  * and written back in the input's orientation.
  *   in[i]   device f32 [rows[i]][cols[i]]   (host array of device pointers)
  *   out[i]  device f32 [rows[i]][cols[i]]   (may not alias in[i])
- * The three products per step run on tcgen05 tensor cores with bf16
- * operands and fp32 accumulation (X, A and B held in bf16); for large
- * batches the Gram matrix and A A use only the upper tiles (both are
- * symmetric).  Any shape; pointers must be 4-byte aligned (float).  Rows
+ * The three products per step run on tcgen05 tensor cores with 16-bit
+ * operands and fp32 accumulation: the unscaled input is held in bf16 (any
+ * magnitude fits), every normalised X, A and B after it in fp16 (11
+ * significant bits; all of them stay far inside fp16's range), except the
+ * first B, which meets the bf16 input in the first product and is bf16
+ * too.  For large batches the Gram matrix and A A use only the upper tiles
+ * (both are symmetric).  Any shape; pointers must be 4-byte aligned (float).  Rows
  * with cols % 4 == 0 and 16-byte aligned pointers are read and written
  * with 16-byte vectors, other shapes element by element.
  */

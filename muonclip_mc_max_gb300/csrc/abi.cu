@@ -758,6 +758,7 @@ mc_status run_mat_pass(const NsPlan& P, int mode, float* const* w, const float* 
         B.lr = lr;
         B.wd = wd;
         B.nesterov = nesterov;
+        B.x_f16 = mode >= 2 && !zero_steps ? 1 : 0;
         B.info = mode <= 1 ? P.info : nullptr;
         B.info_base = c0;
         int tiles = 0;
@@ -827,16 +828,30 @@ bool ns_problem(GemmProblem& q, const NsPlan& P, const NsGroup& gr, int kind, in
     const uint64_t cnt = gr.idx.size(), mp = gr.m_pad, np = gr.n_pad;
     q.batch = (int)cnt;
     q.vec_ok = 1;
+    // Number formats.  The momentum pass writes X unscaled in bf16 (any
+    // magnitude fits).  Every later X, A and B is bounded (normalised X,
+    // |entries| below about 12), and those are held in fp16: its 11
+    // significant bits keep the iteration within a few 1e-3 of the fp64
+    // result where bf16's 8 reached 2e-2 on thin matrices.  Both operands of
+    // one MMA share a type, so the first iteration converts on its outputs:
+    //   Gram 0  bf16 X  -> fp16 A (scaled by s^2)
+    //   poly 0  fp16 A  -> bf16 B (B meets the bf16 X in the apply)
+    //   apply 0 bf16 B, X -> fp16 X (scaled by s)
+    // and every later GEMM reads and writes fp16.
+    const int in_f16 = it == 0 ? (kind == 1) : 1;
+    const int out_f16 = it == 0 ? (kind != 1) : 1;
+    q.ab_f16 = in_f16;  // the aux operand (A in poly, X in apply) has the same type
+    q.out_kind = out_f16 ? kOutF16 : kOutBF16;
     // workspace buffers: 256-byte aligned, rows of m_pad / n_pad (multiples of 64) elements
     q.bulk_st = kind == 2 || !sym;
     if (q.bulk_st) {
         const void* out = kind == 0 ? (const void*)gr.A : kind == 1 ? (const void*)gr.Bm : (const void*)gr.X[xout];
         const uint64_t on = kind == 2 ? np : mp;
-        if (!make_tmap_3d(&q.tmC, out, on, mp, cnt, on, mp * on, 64, 32, 0)) return false;
+        if (!make_tmap_3d(&q.tmC, out, on, mp, cnt, on, mp * on, 64, 32, out_f16)) return false;
     }
     if (kind == 0) {
-        if (!make_tmap_3d(&q.tmA, gr.X[xin], np, mp, cnt, np, mp * np, kBK, kBM, 0)) return false;
-        if (!make_tmap_3d(&q.tmB, gr.X[xin], np, mp, cnt, np, mp * np, kBK, brows, 0)) return false;
+        if (!make_tmap_3d(&q.tmA, gr.X[xin], np, mp, cnt, np, mp * np, kBK, kBM, in_f16)) return false;
+        if (!make_tmap_3d(&q.tmB, gr.X[xin], np, mp, cnt, np, mp * np, kBK, brows, in_f16)) return false;
         q.M = q.N = (int)mp;
         q.K = (int)np;
         q.sym = sym;
@@ -846,8 +861,8 @@ bool ns_problem(GemmProblem& q, const NsPlan& P, const NsGroup& gr, int kind, in
         q.alpha = 1.f;
         q.scale = it == 0 ? P.s2 + gr.zbase : nullptr;
     } else if (kind == 1) {
-        if (!make_tmap_3d(&q.tmA, gr.A, mp, mp, cnt, mp, mp * mp, kBK, kBM, 0)) return false;
-        if (!make_tmap_3d(&q.tmB, gr.A, mp, mp, cnt, mp, mp * mp, kBK, brows, 0)) return false;
+        if (!make_tmap_3d(&q.tmA, gr.A, mp, mp, cnt, mp, mp * mp, kBK, kBM, in_f16)) return false;
+        if (!make_tmap_3d(&q.tmB, gr.A, mp, mp, cnt, mp, mp * mp, kBK, brows, in_f16)) return false;
         q.M = q.N = q.K = (int)mp;
         q.sym = sym;
         q.out = gr.Bm;
@@ -859,8 +874,8 @@ bool ns_problem(GemmProblem& q, const NsPlan& P, const NsGroup& gr, int kind, in
         q.alpha = c;
         q.beta = b;
     } else {
-        if (!make_tmap_3d(&q.tmA, gr.Bm, mp, mp, cnt, mp, mp * mp, kBK, kBM, 0)) return false;
-        if (!make_tmap_3d(&q.tmB, gr.X[xin], np, mp, cnt, np, mp * np, 64, kStageK, 0)) return false;
+        if (!make_tmap_3d(&q.tmA, gr.Bm, mp, mp, cnt, mp, mp * mp, kBK, kBM, in_f16)) return false;
+        if (!make_tmap_3d(&q.tmB, gr.X[xin], np, mp, cnt, np, mp * np, 64, kStageK, in_f16)) return false;
         q.b_mn = 1;
         q.M = (int)mp;
         q.N = (int)np;

@@ -311,8 +311,14 @@ __global__ void __launch_bounds__(kMatThreads) mat_pass_kernel(const __grid_cons
             for (int p = 0; p < 4; ++p) {
                 const int li = p * 16 + (tid >> 4), lj = (tid & 15) * 4;
                 uint2 pk = *reinterpret_cast<const uint2*>(d.x + (size_t)(i0 + li) * d.n_pad + j0 + lj);
-                float2 a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&pk.x));
-                float2 b = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&pk.y));
+                float2 a, b;
+                if (B.x_f16) {
+                    a = __half22float2(*reinterpret_cast<__half2*>(&pk.x));
+                    b = __half22float2(*reinterpret_cast<__half2*>(&pk.y));
+                } else {
+                    a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&pk.x));
+                    b = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&pk.y));
+                }
                 U[li][lj] = a.x;
                 U[li][lj + 1] = a.y;
                 U[li][lj + 2] = b.x;

@@ -206,9 +206,10 @@ MC_D void epilogue_chunk(const GemmProblem& q, int z, int r, int col0, float* f,
         for (int v = 0; v < 8; ++v) {
             uint4 u = *reinterpret_cast<const uint4*>(ap + 8 * v);
             const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+            const __half2* hf = reinterpret_cast<const __half2*>(&u);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                float2 a2 = __bfloat1622float2(h[i]);
+                const float2 a2 = q.ab_f16 ? __half22float2(hf[i]) : __bfloat1622float2(h[i]);
                 f[8 * v + 2 * i] = sc * (q.alpha * f[8 * v + 2 * i] + q.beta * a2.x);
                 f[8 * v + 2 * i + 1] = sc * (q.alpha * f[8 * v + 2 * i + 1] + q.beta * a2.y);
             }
@@ -331,6 +332,10 @@ MC_D void chunk_values(const GemmProblem& q, int row0, int col0, float* f, float
         }
     }
     if (q.aux) {
+        // the problem's fields live in shared memory: read before the stores
+        // to S, which the compiler must assume may alias them
+        const bool aux_f16 = q.ab_f16 != 0;
+        const float alpha = q.alpha, beta = q.beta;
 #pragma unroll
         for (int it = 0; it < 8; ++it) *reinterpret_cast<uint4*>(S + stage_off(swz, it * 4 + sub, seg)) = u[it];
         __syncwarp();
@@ -338,11 +343,13 @@ MC_D void chunk_values(const GemmProblem& q, int row0, int col0, float* f, float
         for (int v = 0; v < 8; ++v) {
             uint4 w = *reinterpret_cast<const uint4*>(S + stage_off(swz, lane, v));
             const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+            const __half2* hf = reinterpret_cast<const __half2*>(&w);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                float2 a2 = __bfloat1622float2(h[i]);
-                f[8 * v + 2 * i] = sc * (q.alpha * f[8 * v + 2 * i] + q.beta * a2.x);
-                f[8 * v + 2 * i + 1] = sc * (q.alpha * f[8 * v + 2 * i + 1] + q.beta * a2.y);
+                // aux has the operands' type (fp16 or bf16)
+                const float2 a2 = aux_f16 ? __half22float2(hf[i]) : __bfloat1622float2(h[i]);
+                f[8 * v + 2 * i] = sc * (alpha * f[8 * v + 2 * i] + beta * a2.x);
+                f[8 * v + 2 * i + 1] = sc * (alpha * f[8 * v + 2 * i + 1] + beta * a2.y);
             }
         }
         __syncwarp();
@@ -375,10 +382,11 @@ MC_D void epilogue_chunk_staged(const GemmProblem& q, int z, int row0, int col0,
     if (q.aux && next_col0 >= 0 && next_col0 < q.N) aux_load(q, z, row0, next_col0, u);
     const bool f16 = q.out_kind == kOutF16;
     if (f16) {
-        bool big = false;
+        // the largest magnitude against the fp16 range (NaN is not a range error)
+        float mx = 0.f;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) big |= fabsf(f[i]) > 65504.0f;
-        if (big) set_status(status, MC_DEV_RANGE);
+        for (int i = 0; i < 64; i += 2) mx = fmaxf(mx, fmaxf(fabsf(f[i]), fabsf(f[i + 1])));
+        if (mx > 65504.0f) set_status(status, MC_DEV_RANGE);
     }
     if (q.bulk_st) {
         // the 32 x 64 box in the swizzled layout of the tensor store (each

@@ -208,7 +208,8 @@ struct MatDesc {
     float* w;            // mode 2: weights [rows][cols] f32 (updated); mode 3: output O
     const float* g;      // mode 0: gradient [rows][cols]
     float* m;            // mode 0: momentum (updated); mode 1: the Newton-Schulz input
-    __nv_bfloat16* x;    // [m_pad][n_pad] bf16 workspace in X orientation
+    __nv_bfloat16* x;    // [m_pad][n_pad] workspace in X orientation: bf16 (modes 0/1; modes 2/3
+                         // with zero NS steps), fp16 (modes 2/3: the Newton-Schulz output)
     double* partial;     // modes 0/1: per-tile sums of squares
     const float* oscale; // modes 2/3: optional device scale of O (zero NS steps)
     float rms;           // mode 2: rms_coef * sqrt(max(rows, cols))
@@ -224,6 +225,7 @@ struct MatBatch {
     int count, total_tiles;
     float mu, lr, wd;
     int nesterov, mode;  // 0 momentum + cast, 1 cast only, 2 update W, 3 write O
+    int x_f16;           // modes 2/3: X holds fp16 (the Newton-Schulz output)
 };
 cudaError_t launch_mat_pass(const MatBatch& b, cudaStream_t stream);
 

@@ -91,6 +91,39 @@ def test_muon_batch_mixed_and_resume():
                        rw - W[i].double().numpy()) < NS_RTOL
 
 
+def test_muon_step_many_groups_and_matrices():
+    """42 matrices in seven padded-shape groups: more groups than one
+    Newton-Schulz launch holds (the launch is split by group) and more
+    matrices than one elementwise pass holds (the passes are split by
+    matrix); every matrix against the oracle."""
+    lib()
+    from muonclip_mc_max_gb300 import api
+    groups = [
+        [(32, 64), (64, 32), (50, 60), (60, 50), (10, 20), (64, 64), (1, 64)],          # 256 x 64
+        [(100, 130), (130, 100), (129, 191), (191, 129), (70, 180), (180, 70), (2, 150)],  # 256 x 192
+        [(60, 600), (600, 60), (90, 580), (580, 90), (5, 640), (640, 5), (200, 590)],   # 256 x 640
+        [(17, 1000), (1000, 17), (40, 990), (990, 40), (8, 1024), (1024, 8), (3, 970)],  # 256 x 1024
+        [(250, 260), (260, 250), (256, 300), (300, 256), (200, 290), (290, 200), (256, 320)],  # 256 x 320
+        [(300, 320), (320, 300), (270, 300), (300, 270), (260, 310), (310, 260)],  # 512 x 320
+        [(400, 300)],                                                                      # 512 x 448
+    ]
+    shapes = [s for g in groups for s in g]
+    assert len(shapes) == 42
+    W = [mc_inputs.matrix(r, c, seed=700 + i, std=0.02) for i, (r, c) in enumerate(shapes)]
+    G = [mc_inputs.matrix(r, c, seed=800 + i, std=1e-3) for i, (r, c) in enumerate(shapes)]
+    M = [mc_inputs.matrix(r, c, seed=900 + i, std=1e-3) for i, (r, c) in enumerate(shapes)]
+    wd_ = [t.to(dev()) for t in W]
+    md = [t.to(dev()) for t in M]
+    api.mc_muon_step(wd_, [t.to(dev()) for t in G], md, lr=2e-4)
+    torch.cuda.synchronize()
+    assert api.mc_read_device_status(clear=True) == 0
+    for i in range(len(shapes)):
+        rw, rm, _ = oracle.muon_step(W[i], G[i], M[i], lr=2e-4)
+        assert rel_fro(md[i].cpu().numpy(), rm) < 1e-6, shapes[i]
+        assert rel_fro(wd_[i].cpu().double().numpy() - W[i].double().numpy(),
+                       rw - W[i].double().numpy()) < NS_RTOL, shapes[i]
+
+
 def test_lr_zero_leaves_weights_bit_unchanged():
     lib()
     from muonclip_mc_max_gb300 import api
