@@ -95,7 +95,10 @@ def test_muon_step_many_groups_and_matrices():
     """42 matrices in seven padded-shape groups: more groups than one
     Newton-Schulz launch holds (the launch is split by group) and more
     matrices than one elementwise pass holds (the passes are split by
-    matrix); every matrix against the oracle."""
+    matrix); every matrix against the oracle.  Beside the 2e-2 contract,
+    matrices with min(rows, cols) >= 8 must stay within 6e-3: the fp16
+    iterates measure at most 4.5e-3 there, where bf16 iterates gave 1-2.2%
+    (990 x 40 broke the contract)."""
     lib()
     from muonclip_mc_max_gb300 import api
     groups = [
@@ -120,8 +123,10 @@ def test_muon_step_many_groups_and_matrices():
     for i in range(len(shapes)):
         rw, rm, _ = oracle.muon_step(W[i], G[i], M[i], lr=2e-4)
         assert rel_fro(md[i].cpu().numpy(), rm) < 1e-6, shapes[i]
-        assert rel_fro(wd_[i].cpu().double().numpy() - W[i].double().numpy(),
-                       rw - W[i].double().numpy()) < NS_RTOL, shapes[i]
+        err = rel_fro(wd_[i].cpu().double().numpy() - W[i].double().numpy(), rw - W[i].double().numpy())
+        assert err < NS_RTOL, shapes[i]
+        if min(shapes[i]) >= 8:
+            assert err < 6e-3, (shapes[i], err)
 
 
 def test_lr_zero_leaves_weights_bit_unchanged():
