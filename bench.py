@@ -34,6 +34,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -385,7 +386,9 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        # the raw samples (the JSON line carries their summary)
+        self.path = os.path.join(os.environ.get("MC_CLOCKS_DIR", tempfile.gettempdir()),
+                                 f"mc_clocks_bench_{os.getpid()}.csv")
 
     def start(self):
         try:
