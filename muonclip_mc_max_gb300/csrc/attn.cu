@@ -4,21 +4,22 @@
 // max logit of this step and leaves the forward unchanged) costs one max per
 // logit on top of O = softmax(Q K^T / sqrt(dh)) V.
 //
-// Work item = (sequence b, head h, 128-query tile); one persistent CTA per
-// SM; items in bands of (b, h) pairs dealt in snake-ordered rounds (as in
-// the scan).  Per 128-key block j of an item:
-//   warp 0      TMA: the item's Q tile once, the K_j and V_j tiles (128 keys
-//               x dh) into a ring of stages
-//   warp 1      tcgen05.mma S_j = Q K_j^T into one of two 128 x 128 fp32
-//               TMEM tiles; once P_j is ready, O += P_j V_j into the
-//               128 x dh fp32 TMEM accumulator (P from shared memory, V
-//               MN-major as stored)
-//   warps 2..5  one query row per lane: S_j from TMEM, the raw row max (for
-//               S_max), the running softmax max m and sum l, O rescaled by
-//               2^(m_old - m_new) in TMEM when m grows, P_j = 2^(s - m) as
-//               bf16 into a swizzled shared tile; at the end of the item
-//               O / l as bf16 and one atomicMax per warp on the monotonic key
-//               of (b, h)
+// Work item = (sequence b, head h, pair of 128-query tiles); one persistent
+// CTA per SM; items in bands of (b, h) pairs dealt in snake-ordered rounds
+// (as in the scan).  Per 128-key block j of an item:
+//   warp 0      TMA: both Q tiles once, then the K_j tiles (128 keys x dh)
+//               into a K ring
+//   warp 2      TMA: the V_j tiles into a V ring
+//   warp 1      tcgen05.mma S_t = Q_t K_j^T for both tiles into two
+//               128 x 128 fp32 TMEM tiles; once P_t is ready, O_t += P_t V
+//               into the tile's 128 x dh fp32 TMEM accumulator (V MN-major
+//               as stored; P_t from TMEM at dh = 64, from shared memory at
+//               dh = 128)
+//   warpgroups 1, 2   one query row per thread of tile 0 / tile 1: S_t from
+//               TMEM, the raw row max (for S_max), the running softmax max m
+//               and sum l, O_t rescaled in TMEM when m moves, P_t = 2^(s - m)
+//               as bf16; at the end of the item O_t / l as bf16 and one
+//               atomicMax per warp on the monotonic key of (b, h)
 // The last CTA turns the keys into S_max (key / sqrt(dh)), like the scan.
 #include "common.cuh"
 #include "internal.h"
@@ -31,12 +32,18 @@ namespace mc {
 //   warpgroup 1  softmax and output of query tile 0 (one row per thread)
 //   warpgroup 2  softmax and output of query tile 1
 // Registers move from warpgroup 0 to the softmax warpgroups with setmaxnreg
-// (128 x 120 + 256 x 184 = 62464 <= 384 threads x 168 at launch); each
-// warpgroup's branch starts with its setmaxnreg, so the compiler allocates
-// the softmax code with 184 registers (128 logits per thread stay in them).
+// (dh = 128: 128 x 120 + 256 x 184 = 62464; dh = 64, where the softmax also
+// packs P for TMEM: 128 x 96 + 256 x 200 = 63488; both <= 384 threads x 168
+// at launch); each warpgroup's branch starts with its setmaxnreg, so the
+// compiler allocates the softmax code with the larger budget (128 logits per
+// thread stay in registers).
 constexpr int kAttnThreads = 384;
-constexpr int kAttnRegsLow = 120, kAttnRegsHigh = 184;
-static_assert(128 * kAttnRegsLow + 256 * kAttnRegsHigh <= kAttnThreads * (65536 / kAttnThreads / 8 * 8),
+template <int DH>
+__host__ __device__ constexpr int attn_regs_low() { return DH == 64 ? 96 : 120; }
+template <int DH>
+__host__ __device__ constexpr int attn_regs_high() { return DH == 64 ? 200 : 184; }
+static_assert(128 * attn_regs_low<64>() + 256 * attn_regs_high<64>() <= kAttnThreads * (65536 / kAttnThreads / 8 * 8) &&
+                  128 * attn_regs_low<128>() + 256 * attn_regs_high<128>() <= kAttnThreads * (65536 / kAttnThreads / 8 * 8),
               "register split");
 constexpr int kAttnBlk = 128;          // queries per tile, keys per key block
 constexpr int kAttnMaxStages = 4;
@@ -131,17 +138,31 @@ MC_D void issue_pv(uint32_t d_tmem, uint64_t pd, uint64_t vd, uint32_t idesc, bo
     }
 }
 
+// dh = 64: P_t in TMEM (one row per lane, two bf16 keys per 32-bit column,
+// 64 columns for 128 keys) as the A operand, 8 columns per K step
+MC_D void issue_pv_tmem_a(uint32_t d_tmem, uint32_t p_tmem, uint64_t vd, uint32_t idesc, bool acc) {
+#pragma unroll
+    for (int k = 0; k < kAttnBlk / 16; ++k) {
+        const uint32_t en = (acc || k != 0) ? 1u : 0u;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "r"(p_tmem + (uint32_t)(k * 8)), "l"(vd + (uint64_t)(k * (2048 >> 4))), "r"(idesc), "r"(en));
+    }
+}
+
 template <uint32_t N>
 MC_D void setmaxnreg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
 template <uint32_t N>
 MC_D void setmaxnreg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
 
+template <int DH>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_constant__ AttnParams P) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     static_assert(sizeof(AttnSmemTail) <= 1024, "tail");
     AttnSmemTail* tail = reinterpret_cast<AttnSmemTail*>(smem);
-    const int nc = P.dh / 64;                 // 64-column blocks per row of q, k, v
+    const int nc = DH / 64;                 // 64-column blocks per row of q, k, v
     uint8_t* sQ = smem + 1024;                // tile t: blocks t*nc ..
     uint8_t* sP = sQ + 2 * nc * kAttnTile;    // tile t: 2 blocks (128 keys) at sP + 2t blocks
     uint8_t* sK = sP + 4 * kAttnTile;         // stage s: nc blocks
@@ -187,7 +208,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     pdl_wait();
 
     if (warp < 4) {
-    setmaxnreg_dec<kAttnRegsLow>();
+    setmaxnreg_dec<attn_regs_low<DH>()>();
     if (warp == 0 || warp == 2) {
         // ---------------- TMA producers: Q and K (warp 0), V (warp 2) ----------------
         if (lane == 0) {
@@ -211,7 +232,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                     mbar_arrive_expect_tx(&tail->qfull, 2 * blk_bytes);
                     for (int t = 0; t < 2; ++t)
                         for (int c = 0; c < nc; ++c)
-                            tma_load_3d(sQ + (t * nc + c) * kAttnTile, &P.tmQ, &tail->qfull, h * P.dh + c * 64,
+                            tma_load_3d(sQ + (t * nc + c) * kAttnTile, &P.tmQ, &tail->qfull, h * DH + c * 64,
                                         (2 * g + t) * kAttnBlk, b);
                 }
                 const int nj = max(njb[0], njb[1]);
@@ -222,7 +243,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                     }
                     mbar_arrive_expect_tx(&full[stage], blk_bytes);
                     for (int c = 0; c < nc; ++c)
-                        tma_load_3d(ring + (stage * nc + c) * kAttnTile, tm, &full[stage], h * P.dh + c * 64,
+                        tma_load_3d(ring + (stage * nc + c) * kAttnTile, tm, &full[stage], h * DH + c * 64,
                                     j * kAttnBlk, b);
                     ++issued[stage];
                     if (++stage == nst) {
@@ -240,7 +261,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         const uint32_t idesc_s = idesc_f16kind(kAttnBlk, kAttnBlk, 0, 0);  // S = Q K^T, K-major K
-        const uint32_t idesc_o = idesc_f16kind(kAttnBlk, P.dh, 1, 0);      // O += P V, MN-major V
+        const uint32_t idesc_o = idesc_f16kind(kAttnBlk, DH, 1, 0);      // O += P V, MN-major V
         int ks = 0, vs = 0;
         uint32_t kph = 0, vph = 0;
         uint32_t sc[2] = {0, 0}, pc[2] = {0, 0}, no[2] = {0, 0}, n = 0;
@@ -263,8 +284,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                 if (!mbar_wait(&tail->pfull[t], pc[t] & 1, abort_flag, P.status)) return false;
                 tc_fence_after();
                 if (lane == 0) {
-                    issue_pv(tmem_base + 256 + t * P.dh, pdesc0 + (uint64_t)(t * ((2 * kAttnTile) >> 4)),
-                             vdesc0 + (uint64_t)vs * blk16, idesc_o, jj != 0);
+                    if (nc == 1)  // P_t in TMEM after O0 and O1
+                        issue_pv_tmem_a(tmem_base + 256 + t * DH, tmem_base + 256 + 2 * DH + t * (kAttnBlk / 2),
+                                        vdesc0 + (uint64_t)vs * blk16, idesc_o, jj != 0);
+                    else
+                        issue_pv(tmem_base + 256 + t * DH, pdesc0 + (uint64_t)(t * ((2 * kAttnTile) >> 4)),
+                                 vdesc0 + (uint64_t)vs * blk16, idesc_o, jj != 0);
                     umma_commit(&tail->oready[t]);
                 }
                 __syncwarp();
@@ -333,14 +358,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         mbar_wait(&tail->drain, 0, &never, P.status);
     }
     } else {
-        setmaxnreg_inc<kAttnRegsHigh>();
+        setmaxnreg_inc<attn_regs_high<DH>()>();
         // ---------------- softmax and output: tile t = warpgroup - 1 ----------------
         const int t = warp >= 8 ? 1 : 0;
         const int quarter = warp & 3;        // TMEM lanes 32 q .. 32 q + 31
         const int lr = quarter * 32 + lane;  // row of the tile
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         const uint32_t tS = tmem_base + lane_base + t * kAttnBlk;
-        const uint32_t tO = tmem_base + lane_base + 256 + t * P.dh;
+        const uint32_t tO = tmem_base + lane_base + 256 + t * DH;
+        const uint32_t tP = tmem_base + lane_base + 256 + 2 * DH + t * (kAttnBlk / 2);  // dh = 64 only
         uint8_t* pt = sP + 2 * t * kAttnTile;
         uint32_t sc = 0, pc = 0;
         bool ok = true;
@@ -411,7 +437,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                     }
                     tc_fence_after();
                     if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
-                        for (int c = 0; c < P.dh / 32; ++c) {
+                        #pragma unroll 1
+                        for (int c = 0; c < DH / 32; ++c) {
                             uint32_t o[32];
                             tmem_ld32(tO + c * 32, o);
                             tmem_ld_wait();
@@ -422,16 +449,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                         tmem_st_wait();
                     }
                 }
-                // P_j as bf16, 128-byte swizzled K-major rows (two 64-key blocks)
+                if constexpr (DH == 64) {
+                    // P_j as bf16 pairs into this row's 64 TMEM columns (the A
+                    // operand of P.V; TMEM holds S, O and P of both tiles at dh = 64)
 #pragma unroll
-                for (int cc = 0; cc < kAttnBlk / 8; ++cc) {
-                    __nv_bfloat162 hh[4];
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint32_t pw[16];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) hh[e] = __floats2bfloat162_rn(v[cc * 8 + 2 * e], v[cc * 8 + 2 * e + 1]);
-                    *reinterpret_cast<uint4*>(pt + (cc >> 3) * kAttnTile + lr * 128 + (((cc & 7) ^ (lr & 7)) << 4)) =
-                        *reinterpret_cast<uint4*>(hh);
+                        for (int e = 0; e < 16; ++e) {
+                            __nv_bfloat162 hh = __floats2bfloat162_rn(v[q4 * 32 + 2 * e], v[q4 * 32 + 2 * e + 1]);
+                            pw[e] = *reinterpret_cast<uint32_t*>(&hh);
+                        }
+                        tmem_st16(tP + q4 * 16, pw);
+                    }
+                    tmem_st_wait();
+                } else {
+                    // P_j as bf16, 128-byte swizzled K-major rows (two 64-key blocks)
+#pragma unroll
+                    for (int cc = 0; cc < kAttnBlk / 8; ++cc) {
+                        __nv_bfloat162 hh[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) hh[e] = __floats2bfloat162_rn(v[cc * 8 + 2 * e], v[cc * 8 + 2 * e + 1]);
+                        *reinterpret_cast<uint4*>(pt + (cc >> 3) * kAttnTile + lr * 128 + (((cc & 7) ^ (lr & 7)) << 4)) =
+                            *reinterpret_cast<uint4*>(hh);
+                    }
+                    fence_proxy_async_smem();
                 }
-                fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tail->pfull[t]);
@@ -442,8 +485,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
             if (!mbar_wait(&tail->oready[t], (pc - 1) & 1, abort_flag, P.status)) break;
             tc_fence_after();
             const float inv = row_ok ? 1.f / l : 0.f;
-            __nv_bfloat16* orow = P.o + ((size_t)b * P.T + (row_ok ? row : 0)) * P.ld + (size_t)h * P.dh;
-            for (int c = 0; c < P.dh / 32; ++c) {
+            __nv_bfloat16* orow = P.o + ((size_t)b * P.T + (row_ok ? row : 0)) * P.ld + (size_t)h * DH;
+            #pragma unroll 1
+            for (int c = 0; c < DH / 32; ++c) {
                 uint32_t o[32];
                 tmem_ld32(tO + c * 32, o);
                 tmem_ld_wait();
@@ -524,7 +568,9 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {
     int dev = current_device();
     if (dev < 0) return cudaErrorInvalidDevice;
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+        cudaError_t e = cudaFuncSetAttribute(attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
@@ -532,7 +578,8 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {
     if (grid > P.total_items) grid = P.total_items;
     P.band = std::max(1, std::min(a.B * a.H, (2 * grid + P.n_pair - 1) / P.n_pair));
     TraceScope ts("attn", stream);
-    return launch_pdl(attn_kernel, dim3(grid), dim3(kAttnThreads), kAttnSmem, stream, P);
+    return nc == 1 ? launch_pdl(attn_kernel<64>, dim3(grid), dim3(kAttnThreads), kAttnSmem, stream, P)
+                   : launch_pdl(attn_kernel<128>, dim3(grid), dim3(kAttnThreads), kAttnSmem, stream, P);
 }
 
 }  // namespace mc
