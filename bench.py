@@ -445,6 +445,23 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest of the ranks' values: in a replica job the slowest rank
+    sets the job's time.  One rank returns x itself."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flops_per_rank: float, seconds: float) -> float:
+    """Whole-job throughput: every rank's algorithmic flops over the job's time."""
+    return world * flops_per_rank / seconds / 1e12
+
+
 def run_reference(args, wl):
     """The fp64 oracle on the host cores: each step is one bounded sample of
     the workload (inputs drawn on the CPU)."""
@@ -525,14 +542,10 @@ def run_ours(args, wl):
     clk = clocks.stop()
     launches = per_step_launches * K
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    tot_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([tot_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_ms = float(t.item())
+    tot_ms = max_over_ranks(sum(step_ms), world, device)
     ms = tot_ms / K
     flops = wl.scan_flops + wl.ns_flops
-    value = world * flops / (ms * 1e-3) / 1e12
+    value = job_tflops(world, flops, ms * 1e-3)
     hbm_peak, bf16_peak, bf16_sus, peak_src = load_peaks()
 
     def part_ms(g):
@@ -640,12 +653,8 @@ def run_ours(args, wl):
     stream.synchronize()
     copy_stream.synchronize()
     barrier()
-    e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e_value = world * flops * K / e2e_s / 1e12
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, device)
+    e2e_value = job_tflops(world, flops * K, e2e_s)
 
     line = None
     if rank == 0:

@@ -1,0 +1,100 @@
+"""Host logic of the N-replica benchmark, run as two gloo ranks on the CPU.
+
+The method's path needs no exchange between GPUs in this build: N GPUs run N
+independent replicas of the step, and the job's time is the slowest rank's.
+These tests check that reduction, the whole-job throughput, and that only
+rank 0 runs and prints the oracle (reference) arm.
+"""
+import io
+import json
+import os
+import socket
+import sys
+import types
+from contextlib import redirect_stdout
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+class _FakeWorkload:
+    """Stands in for a workload in the reference arm: one 'sample' is 2e9
+    flops in 0.5 s.  make() counts its calls so a rank that should do no work
+    can be seen to have done none."""
+    metric = "test metric"
+    desc = "fake workload"
+
+    def __init__(self):
+        self.made = 0
+
+    def make(self, device):
+        self.made += 1
+        return {}
+
+    def oracle_sample(self, s):
+        return 2e9, 0.5, "fake sample"
+
+
+def _rank_main(rank, world, port, out_dir):
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import torch.distributed as dist
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        t = bench.max_over_ranks(10.0 + 5.0 * rank, world)
+        args = types.SimpleNamespace(gpus=world, steps=3, warmup=1)
+        wl = _FakeWorkload()
+        buf = io.StringIO()
+        with redirect_stdout(buf):
+            bench.run_reference(args, wl)
+        dist.barrier()
+        with open(os.path.join(out_dir, f"rank{rank}.json"), "w") as f:
+            json.dump({"t": t, "made": wl.made, "stdout": buf.getvalue()}, f)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_replica_timing_and_reference_arm_on_two_gloo_ranks(tmp_path):
+    mp = pytest.importorskip("torch.multiprocessing")
+    world = 2
+    ctx = mp.get_context("spawn")
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, str(tmp_path))) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+    for p in procs:
+        if p.is_alive():
+            p.kill()
+            p.join()
+    assert [p.exitcode for p in procs] == [0, 0]
+    res = [json.load(open(tmp_path / f"rank{r}.json")) for r in range(world)]
+    # the slowest rank sets the time on every rank
+    assert [r["t"] for r in res] == [15.0, 15.0]
+    # rank 0 alone draws inputs, runs the oracle and prints one JSON line
+    assert res[0]["made"] == 1 and res[1]["made"] == 0
+    assert res[1]["stdout"] == ""
+    lines = res[0]["stdout"].strip().splitlines()
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["steps"] == 3
+    assert line["value"] == pytest.approx(2e9 / 0.5 / 1e12)
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_job_throughput_counts_every_rank():
+    sys.path.insert(0, ROOT)
+    import bench
+    # two replicas of 1e12 flops each in the job's 0.5 s: 4 TFLOP/s
+    assert bench.job_tflops(2, 1e12, 0.5) == pytest.approx(4.0)
+    assert bench.max_over_ranks(3.25, 1) == 3.25
