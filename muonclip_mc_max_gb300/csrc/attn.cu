@@ -276,14 +276,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         const uint64_t blk16 = (uint64_t)(nc * kAttnTile) >> 4;  // one stage or one Q tile
         // O_t += P_t V_jj for both tiles that use key block jj; the first
         // product of an item overwrites O_t once the previous output is read
+        // Each pair of products waits for both tiles' barriers first and is
+        // then issued back to back: this thread's control steps are slow on a
+        // sub-partition shared with two softmax warps, and the tensor pipe
+        // drains during every step between two batches of MMAs.
         auto pv = [&](int jj) {
             if (!mbar_wait(&tail->vfull[vs], vph, abort_flag, P.status)) return false;
             for (int t = 0; t < 2; ++t) {
                 if (jj >= njb[t]) continue;
                 if (jj == 0 && !mbar_wait(&tail->oempty[t], (no[t] & 1) ^ 1, abort_flag, P.status)) return false;
                 if (!mbar_wait(&tail->pfull[t], pc[t] & 1, abort_flag, P.status)) return false;
-                tc_fence_after();
-                if (lane == 0) {
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                for (int t = 0; t < 2; ++t) {
+                    if (jj >= njb[t]) continue;
                     if (nc == 1)  // P_t in TMEM after O0 and O1
                         issue_pv_tmem_a(tmem_base + 256 + t * DH, tmem_base + 256 + 2 * DH + t * (kAttnBlk / 2),
                                         vdesc0 + (uint64_t)vs * blk16, idesc_o, jj != 0);
@@ -292,12 +299,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                                  vdesc0 + (uint64_t)vs * blk16, idesc_o, jj != 0);
                     umma_commit(&tail->oready[t]);
                 }
-                __syncwarp();
+                umma_commit(&tail->vempty[vs]);  // V_jj consumed by both tiles
+            }
+            __syncwarp();
+            for (int t = 0; t < 2; ++t) {
+                if (jj >= njb[t]) continue;
                 ++pc[t];
                 if (jj == njb[t] - 1) ++no[t];
             }
-            if (lane == 0) umma_commit(&tail->vempty[vs]);  // V_jj consumed by both tiles
-            __syncwarp();
             if (++vs == P.vst) {
                 vs = 0;
                 vph ^= 1;
@@ -317,12 +326,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                 }
                 for (int t = 0; t < 2 && ok; ++t) {
                     if (j >= njb[t]) continue;
-                    if (!mbar_wait(&tail->sempty[t], (sc[t] & 1) ^ 1, abort_flag, P.status)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    if (lane == 0) {
+                    if (!mbar_wait(&tail->sempty[t], (sc[t] & 1) ^ 1, abort_flag, P.status)) ok = false;
+                }
+                if (!ok) break;
+                tc_fence_after();
+                if (lane == 0) {
+                    for (int t = 0; t < 2; ++t) {
+                        if (j >= njb[t]) continue;
                         const uint64_t qd = qdesc0 + (uint64_t)t * blk16, kd = kdesc0 + (uint64_t)ks * blk16;
                         if (nc == 1)
                             issue_s<1>(tmem_base + t * kAttnBlk, qd, kd, idesc_s);
@@ -330,15 +340,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                             issue_s<2>(tmem_base + t * kAttnBlk, qd, kd, idesc_s);
                         umma_commit(&tail->sfull[t]);
                     }
-                    __syncwarp();
-                    ++sc[t];
-                }
-                if (!ok) break;
-                if (lane == 0) {
                     umma_commit(&tail->kempty[ks]);                // K_j consumed
                     if (j == nj - 1) umma_commit(&tail->qempty);  // the item's last use of Q
                 }
                 __syncwarp();
+                for (int t = 0; t < 2; ++t)
+                    if (j < njb[t]) ++sc[t];
                 if (++ks == P.kst) {
                     ks = 0;
                     kph ^= 1;
