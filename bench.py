@@ -71,7 +71,7 @@ TRAFFIC = {
     ("c2", "scan"): 33612544,
     ("c3", "scan"): 2933748736 + 143360,
     ("c5", "scan"): 1450577664 + 3536896,
-    ("attn", "attn"): 50551808 + 818688,
+    ("attn", "attn"): 50556416 + 814080,
 }
 
 
