@@ -292,6 +292,26 @@ mc_status mc_gemm_bf16(const void* a, const void* b, void* c, mc_dtype c_type, i
                        int K, int batch, int b_kmajor, mc_stream_t stream);
 
 /* ======================================================================
+ * Failure detection self-test (no counterpart on the pages: it checks the
+ * library's own bounded waits)
+ * ====================================================================== */
+
+/* Every on-chip wait of the library is bounded: after 1 s it sets
+ * MC_DEV_TIMEOUT, raises its CTA's abort flag (so the CTA's other waits end
+ * too) and the kernel returns.  This call launches one CTA whose two warps
+ * wait, through that same code, on barriers that nothing completes: warp 0
+ * gives up after limit_us microseconds (1 .. 1000000), warp 1 (normal
+ * limit) must leave on warp 0's abort flag.
+ *   out  device, 8-byte aligned, 4 x int64, written by the kernel:
+ *        out[0], out[1] = each warp's wait in ns; out[2], out[3] = 1 if its
+ *        barrier completed (never, when the waits work).
+ * Expected afterwards: MC_DEV_TIMEOUT in mc_read_device_status, out[0] just
+ * above limit_us, out[1] well below 1 s, and a usable context.  Returns
+ * MC_ERR_INVALID_ARG (nothing launched) for a limit out of range or a null
+ * or misaligned out.  Asynchronous on `stream`. */
+mc_status mc_selftest_wait_timeout(unsigned limit_us, long long* out, mc_stream_t stream);
+
+/* ======================================================================
  * Tracing (no counterpart on the pages: observability of the library)
  * ====================================================================== */
 

@@ -25,7 +25,7 @@ __all__ = [
     "mc_qk_clip_mha", "mc_qk_clip_mla", "mc_qk_clip_global",
     "mc_newton_schulz", "mc_newton_schulz_workspace_size",
     "mc_muon_step", "mc_muon_workspace_size", "mc_gemm_bf16",
-    "mc_launch_count", "mc_trace_enable", "mc_trace_collect",
+    "mc_launch_count", "mc_trace_enable", "mc_trace_collect", "mc_selftest_wait_timeout",
     "MC_F32", "MC_BF16", "MC_DEV_NONFINITE", "MC_DEV_TIMEOUT", "MC_DEV_RANGE", "NS_COEFFS",
 ]
 
@@ -98,6 +98,7 @@ def load_library():
         "mc_newton_schulz": ([VP, VP, IP, IP, I, I, F, F, F, F, V, S, V], I),
         "mc_muon_step": ([VP, VP, VP, IP, IP, I, F, F, F, F, I, F, F, F, F, I, V, S, V], I),
         "mc_gemm_bf16": ([V, V, V, I, I, I, I, I, I, V], I),
+        "mc_selftest_wait_timeout": ([U, V, V], I),
         "mc_launch_count": ([], ctypes.c_ulonglong),
         "mc_trace_enable": ([I], I),
         "mc_trace_collect": ([ctypes.POINTER(TraceEntry), I, I], I),
@@ -414,6 +415,21 @@ def mc_gemm_bf16(a, b, b_kmajor: bool = True, out_dtype=torch.float32, out=None,
 # ---------------------------------------------------------------------------
 # tracing
 # ---------------------------------------------------------------------------
+
+def mc_selftest_wait_timeout(limit_us: int = 20000, out=None, stream=None):
+    """Bounded-wait self-test: one CTA whose warps wait on barriers nothing
+    completes; returns the device int64[4] result (the two warps' waits in
+    ns, then two completion flags).  Read MC_DEV_TIMEOUT with
+    mc_read_device_status afterwards."""
+    lib = load_library()
+    _need_cuda(out)
+    if out is None:
+        out = torch.zeros(4, dtype=torch.int64, device=torch.device("cuda", torch.cuda.current_device()))
+    elif out.dtype != torch.int64 or out.numel() < 4:
+        raise ValueError("out must hold 4 int64 values")
+    _check("mc_selftest_wait_timeout", lib.mc_selftest_wait_timeout(int(limit_us), _ptr(out), _stream(stream)))
+    return out
+
 
 def mc_launch_count() -> int:
     """Kernels launched by the library so far in this process."""

@@ -263,6 +263,13 @@ mc_status mc_read_device_status(mc_stream_t stream, unsigned* bits, int clear) {
     return MC_OK;
 }
 
+mc_status mc_selftest_wait_timeout(unsigned limit_us, long long* out, mc_stream_t stream) {
+    if (limit_us < 1 || limit_us > 1000000u || !out || (reinterpret_cast<uintptr_t>(out) & 7))
+        return MC_ERR_INVALID_ARG;
+    MC_CUDA(launch_wait_selftest((uint64_t)limit_us * 1000ull, out, (cudaStream_t)stream));
+    return MC_OK;
+}
+
 unsigned long long mc_launch_count(void) { return g_launches.load(); }
 
 mc_status mc_trace_enable(int on) {

@@ -123,14 +123,15 @@ MC_D bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Bounded wait on an mbarrier phase.  Returns false (and flags the status
 // word and the CTA's abort flag) when the limit expires or another role of
 // the CTA has already aborted.
-MC_D bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, unsigned* status) {
+MC_D bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, unsigned* status,
+                    uint64_t limit_ns = kWaitLimitNs) {
     uint32_t b = smem_u32(bar);
     if (mbar_try_wait(b, parity)) return true;
     uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(b, parity)) return true;
         if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             *abort_flag = 1;
             set_status(status, MC_DEV_TIMEOUT);
             return false;

@@ -401,4 +401,39 @@ cudaError_t launch_norm_finalize(const NormArgs& a, cudaStream_t stream) {
     return launch_pdl(norm_finalize_kernel, dim3(a.count), dim3(256), 0, stream, a);
 }
 
+// ---------------------------------------------------------------------------
+// Self-test of the bounded on-chip waits: both warps of one CTA wait on
+// mbarriers that nothing arrives on, through the same wait as every kernel
+// of the library.  Warp 0 gives up after limit_ns (setting MC_DEV_TIMEOUT and
+// the CTA's abort flag); warp 1, with the library's normal limit, must then
+// leave through the abort flag.  out[w] = warp w's wait in ns, out[2 + w] = 1
+// if its barrier completed (it cannot).  Every path ends: no hang, no fault.
+// ---------------------------------------------------------------------------
+__global__ void wait_selftest_kernel(uint64_t limit_ns, long long* out, unsigned* status) {
+    __shared__ __align__(8) uint64_t bar[2];
+    __shared__ int abort_flag;
+    pdl_wait();
+    if (threadIdx.x == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5;
+    const uint64_t t0 = globaltimer_ns();
+    const bool done = mbar_wait(&bar[warp], 0, &abort_flag, status, warp == 0 ? limit_ns : kWaitLimitNs);
+    const uint64_t t1 = globaltimer_ns();
+    if ((threadIdx.x & 31) == 0) {
+        out[warp] = (long long)(t1 - t0);
+        out[2 + warp] = done ? 1 : 0;
+    }
+    pdl_trigger();
+}
+
+cudaError_t launch_wait_selftest(uint64_t limit_ns, long long* out, cudaStream_t stream) {
+    TraceScope ts("selftest_wait", stream);
+    return launch_pdl(wait_selftest_kernel, dim3(1), dim3(64), 0, stream, limit_ns, out, device_status_ptr());
+}
+
 }  // namespace mc

@@ -228,6 +228,8 @@ struct MatBatch {
     int x_f16;           // modes 2/3: X holds fp16 (the Newton-Schulz output)
 };
 cudaError_t launch_mat_pass(const MatBatch& b, cudaStream_t stream);
+// bounded-wait self-test (one CTA of two waiting warps; elementwise.cu)
+cudaError_t launch_wait_selftest(uint64_t limit_ns, long long* out, cudaStream_t stream);
 
 // s[z] = 1 / (sqrt(sum partial[z]) + eps), s2[z] = s[z]^2
 struct NormArgs {

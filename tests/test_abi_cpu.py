@@ -81,6 +81,11 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert lib.mc_attention_mha(q, k, v, 1, 8, 2, 64, 0, 0, o, fake, nil, ws, 4, nil) == 4
     assert lib.mc_attention_mha(q, k, v, 1, 8, 2, 64, 0, 0, o, fake, nil, ctypes.c_void_p(4100), big,
                                 nil) == 4
+    # bounded-wait self-test: limit out of range, null or misaligned result
+    assert lib.mc_selftest_wait_timeout(0, fake, nil) == 1
+    assert lib.mc_selftest_wait_timeout(1000001, fake, nil) == 1
+    assert lib.mc_selftest_wait_timeout(1000, nil, nil) == 1
+    assert lib.mc_selftest_wait_timeout(1000, ctypes.c_void_p(4100), nil) == 1
 
 
 def test_workspace_sizes(lib):
