@@ -162,6 +162,11 @@ class Workspace:
         return self.buf
 
 
+# One default scratch buffer per device, used by every call that passes no
+# workspace.  Calls are stream-ordered on it, so calls issued concurrently on
+# different streams must each pass their own Workspace; a buffer grows (and
+# its old storage returns to torch's allocator) only between calls, never
+# while a CUDA graph is being captured once the graph's calls have run once.
 _default_ws: dict = {}
 
 
