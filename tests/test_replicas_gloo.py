@@ -98,3 +98,23 @@ def test_job_throughput_counts_every_rank():
     # two replicas of 1e12 flops each in the job's 0.5 s: 4 TFLOP/s
     assert bench.job_tflops(2, 1e12, 0.5) == pytest.approx(4.0)
     assert bench.max_over_ranks(3.25, 1) == 3.25
+
+
+def test_reference_arm_prints_one_contract_line():
+    """The oracle arm of the benchmark on the default workload, one bounded
+    sample: one JSON line with the keys the benchmark contract names."""
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "0"], capture_output=True, text=True,
+                       timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e", "impl"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0 and line["steps"] == 1
+    assert line["config"]["workload"].startswith("MHA layer")
+    assert line["cpu_baseline"]["value"] == line["value"]
