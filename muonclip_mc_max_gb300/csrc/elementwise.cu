@@ -4,6 +4,7 @@
 //     tall matrices) with a deterministic per-tile sum of squares
 //   * Frobenius-norm finalisation
 //   * the RMS-matched, weight-decayed update W <- W - lr (rms O + wd W)
+//   * the self-test of the bounded on-chip waits (one small CTA)
 // All loads and stores are 128-bit where the layout allows.
 #include "common.cuh"
 #include "internal.h"

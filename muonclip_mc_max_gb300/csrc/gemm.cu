@@ -4,13 +4,13 @@
 // tiles drawn from up to four problems per phase (projections of one layer,
 // or one Newton-Schulz phase over every matrix of a batch).
 //   warps 0, 6  TMA producers: warp 0 loads the A half of every stage, warp
-//               6 the B half (bf16, 128-byte swizzle, K = 128 per stage in
-//               two 64-wide chunks) into a 3-stage ring
+//               6 the B half (bf16 or fp16, 128-byte swizzle, K = 128 per
+//               stage in two 64-wide chunks) into a 3-stage ring
 //   warp 1      TMEM owner and MMA issuer: 8 x tcgen05.mma (K = 16) per
 //               stage, one commit per stage, into one of two fp32 TMEM
 //               accumulators
-//   warps 2..5  epilogue: tcgen05.ld -> scale / aux / RoPE -> bf16 or f32
-//               global stores (mirrored for symmetric outputs)
+//   warps 2..5  epilogue: tcgen05.ld -> scale / aux / RoPE -> bf16, fp16
+//               or f32 global stores (mirrored for symmetric outputs)
 // The double-buffered accumulator lets the epilogue of tile t overlap the
 // MMAs of tile t+1.  Every wait is bounded (see mbar_wait).
 #include "common.cuh"
