@@ -445,6 +445,24 @@ def dist_env():
     return world, rank, local
 
 
+def clip_summary(s) -> dict | None:
+    """S_max, gamma and the number of clipped heads (gamma < 1) that the last
+    step left in workload state s; None for a workload without a scan."""
+    if "s_max" not in s:
+        return None
+    sm = s["s_max"].detach().float().cpu()
+    res = {"heads": int(sm.numel()), "s_max_max": float(sm.max()), "s_max_min": float(sm.min())}
+    if s.get("tau") is not None:
+        res["tau"] = float(s["tau"])
+    if "gamma" in s:
+        g = s["gamma"].detach().float().cpu()
+        res["clipped_heads"] = int((g < 1).sum())
+        res["gamma_min"] = float(g.min())
+    if s.get("hot") is not None:
+        res["planted_hot_heads"] = [int(h) for h in s["hot"]]
+    return res
+
+
 def max_over_ranks(x: float, world: int, device=None) -> float:
     """The largest of the ranks' values: in a replica job the slowest rank
     sets the job's time.  One rank returns x itself."""
@@ -540,6 +558,7 @@ def run_ours(args, wl):
         ev[k][1].record(stream)
     barrier()
     clk = clocks.stop()
+    clip = clip_summary(s)  # the last timed step's S_max and gamma
     launches = per_step_launches * K
     step_ms = [a.elapsed_time(b) for a, b in ev]
     tot_ms = max_over_ranks(sum(step_ms), world, device)
@@ -691,6 +710,8 @@ def run_ours(args, wl):
                     "d2h_bytes_per_step": d2h},
             "cpu_baseline": cpu,
         }
+        if clip is not None:
+            line["clip"] = clip
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

@@ -1,9 +1,11 @@
-"""Host logic of the N-replica benchmark, run as two gloo ranks on the CPU.
+"""Host logic of the benchmark, on the CPU.
 
-The method's path needs no exchange between GPUs in this build: N GPUs run N
+The method's path needs no exchange between GPUs here: N GPUs run N
 independent replicas of the step, and the job's time is the slowest rank's.
-These tests check that reduction, the whole-job throughput, and that only
-rank 0 runs and prints the oracle (reference) arm.
+Two gloo ranks check that reduction, the whole-job throughput, and that only
+rank 0 runs and prints the oracle (reference) arm; the oracle arm's line is
+checked for the contract's keys, and the S_max / gamma report of the bench
+line is checked on known values.
 """
 import io
 import json
@@ -118,3 +120,21 @@ def test_reference_arm_prints_one_contract_line():
     assert line["impl"] == "reference" and line["value"] > 0 and line["steps"] == 1
     assert line["config"]["workload"].startswith("MHA layer")
     assert line["cpu_baseline"]["value"] == line["value"]
+
+
+def test_clip_summary_of_the_last_step():
+    """The bench line's S_max / gamma report: heads whose gamma < 1 are
+    counted as clipped; a workload without a scan reports nothing."""
+    import torch
+    sys.path.insert(0, ROOT)
+    import bench
+    s = {"s_max": torch.tensor([1.6, 2409.8, 1.4, 2540.7]),
+         "gamma": torch.tensor([1.0, 0.0415, 1.0, 0.0394]), "tau": 100.0, "hot": [1, 3]}
+    r = bench.clip_summary(s)
+    assert r["heads"] == 4 and r["clipped_heads"] == 2 and r["planted_hot_heads"] == [1, 3]
+    assert r["s_max_max"] == pytest.approx(2540.7) and r["gamma_min"] == pytest.approx(0.0394)
+    assert r["tau"] == 100.0
+    json.dumps(r)
+    assert bench.clip_summary({"w": [torch.zeros(2)]}) is None
+    only_smax = bench.clip_summary({"s_max": torch.tensor([3.0, 1.0])})
+    assert only_smax == {"heads": 2, "s_max_max": 3.0, "s_max_min": 1.0}
