@@ -138,3 +138,21 @@ def test_clip_summary_of_the_last_step():
     assert bench.clip_summary({"w": [torch.zeros(2)]}) is None
     only_smax = bench.clip_summary({"s_max": torch.tensor([3.0, 1.0])})
     assert only_smax == {"heads": 2, "s_max_max": 3.0, "s_max_min": 1.0}
+
+
+def test_newton_schulz_flop_accounting():
+    """The bench's Newton-Schulz flop count against the FLOP formula of the
+    Muon blog's "Analysis" section: 2T(2nm^2 + m^3) for T iterations on an
+    m x n matrix counts every product densely.  The algorithmic count of the
+    roofline takes the symmetric Gram and A.A once (m(m+1)n and m^2(m+1));
+    for the expert batch (96 matrices 2048 x 7168, T = 5) the two totals are
+    65.97 and 47.43 TFLOP."""
+    sys.path.insert(0, ROOT)
+    import bench
+    m, n, T = 2048, 7168, 5
+    f = bench.ns_flops_per_iter(m, n)
+    dense = 2 * m * m * n + 2 * m ** 3 + 2 * m * m * n
+    assert T * dense == 2 * T * (2 * n * m * m + m ** 3)
+    assert f["gram"] == m * (m + 1) * n and f["poly"] == m * m * (m + 1) and f["apply"] == 2 * m * m * n
+    assert 96 * T * dense / 1e12 == pytest.approx(65.97, abs=0.01)
+    assert 96 * T * sum(f.values()) / 1e12 == pytest.approx(47.43, abs=0.01)
