@@ -156,3 +156,22 @@ def test_newton_schulz_flop_accounting():
     assert f["gram"] == m * (m + 1) * n and f["poly"] == m * m * (m + 1) and f["apply"] == 2 * m * m * n
     assert 96 * T * dense / 1e12 == pytest.approx(65.97, abs=0.01)
     assert 96 * T * sum(f.values()) / 1e12 == pytest.approx(47.43, abs=0.01)
+
+
+def test_workload_flop_accounting():
+    """Algorithmic work of each bench workload from first principles: a
+    projection is 2 M N K flops, a logit 2 d flops per (i, j) pair (T^2 per
+    sequence, T(T+1)/2 when causal), Newton-Schulz as above (two 1024 x 1024
+    matrices for the MHA layer; W_qa, W_qb, W_kva, W_kb for the long MLA)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    c2 = bench.WORKLOADS["c2"]()
+    assert c2.units["gemm:proj"][1] == 2 * 2 * 8 * 1024 * 1024 * 1024           # 34.4 GF
+    assert c2.units["scan"][1] == 2 * 8 * 1024 * 1024 * 16 * 64                  # 17.2 GF
+    assert c2.ns_flops == 2 * 5 * (2 * 1024 * 1025 * 1024 + 2 * 1024 ** 3)       # 2 x 21.5 GF
+    c3 = bench.WORKLOADS["c3"]()
+    assert c3.scan_flops / 1e12 == pytest.approx(8.307, abs=1e-3)                # 5.008 + 3.299
+    assert c3.units["scan"][1] == 2 * 16 * (4096 * 4097 // 2) * 64 * 192
+    c5 = bench.WORKLOADS["c5"]()
+    assert c5.scan_flops / 1e12 == pytest.approx(15.699, abs=1e-3)               # 2.504 + 13.195
+    assert c5.ns_flops / 1e12 == pytest.approx(0.7945, abs=1e-4)
