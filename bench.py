@@ -1,15 +1,23 @@
 #!/usr/bin/env python
 """MuonClip step benchmark: prints ONE JSON line.
 
-A step is one pass of the whole hot path on one batch of synthetic input:
-max-logit scan (projections + QK^T max), Muon (momentum, 5 quintic
-Newton-Schulz iterations, RMS matching, weight decay) and QK-Clip, through
-the library's C ABI.  Default workload: an MHA layer in bf16, x [8, 1024,
-1024], 16 heads of 64, tau = 100, Muon on the 1024 x 1024 fp32 masters of
-W_q and W_k.
+A step is one pass of the whole hot path on one batch of synthetic input,
+through the library's C ABI.  The default line measures the two K2-scale
+workloads in one process:
+
+  * the headline: Muon on the MoE expert batch -- 48 up-projections
+    7168 x 2048 and 48 down-projections 2048 x 7168, fp32 masters, momentum
+    0.95, 5 quintic Newton-Schulz iterations (16-bit operands, fp32
+    accumulation), RMS matching 0.2 sqrt(max(A,B)), weight decay 0.1
+    (``value``, ``ms_per_step``, ``roofline``, ``e2e``, ``cpu_baseline``);
+  * beside it, the long-context K2 MLA MuonClip step -- x [1, 32768, 7168],
+    64 heads, causal max-logit scan, Muon on W_qa, W_qb, W_kva, W_kb, then
+    the MLA QK-Clip (``muonclip_step_ms``, ``scan_tflops``,
+    ``scan_frac_bf16_peak`` and the object ``long_mla`` with its own
+    roofline and kernel breakdown).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload c2|c3|c4|c5|attn|attnl]
+                  [--workload c4|c2|c3|c5|attn|attnl] [--no-long-mla]
 
 value     = algorithmic TFLOP/s of the step (scan + Newton-Schulz flops per
             step / device time per step, inputs resident, L2 flushed between
@@ -17,10 +25,13 @@ value     = algorithmic TFLOP/s of the step (scan + Newton-Schulz flops per
 e2e       = the same through the public API with the step's inputs copied
             host->device from pinned memory and the results read back;
 roofline  = the dominant kernel's algorithmic work per launch / its
-            event-timed duration against the measured peak;
+            event-timed duration against the measured peak (the sustained
+            bf16 figure for a contraction inside a step of milliseconds that
+            repeats back to back, the burst figure otherwise);
 cpu_baseline = the fp64 oracle on this host's cores on a bounded sample.
 --impl reference times that oracle (the only reference this method has).
 
+c2 is the MHA layer (x [8,1024,1024], 16 heads of 64, Muon on W_q and W_k).
 attn / attnl time the attention forward that takes the max logit along
 (value = its algorithmic TFLOP/s: 4 flops per allowed (i, j) pair and head
 dimension); they are extra lines, not the default workload.
@@ -113,9 +124,16 @@ def load_peaks():
 class Workload:
     name = ""
     desc = ""
+    # a contraction inside a step of milliseconds, repeated back to back,
+    # runs under the power cap: its roofline takes the sustained bf16 peak
+    sustained = False
 
     def make(self, device):
         raise NotImplementedError
+
+    def cpu_state(self):
+        """Host-side inputs of the oracle sample (the reference arm)."""
+        return self.make("cpu")
 
     def step(self, s, api):
         raise NotImplementedError
@@ -204,6 +222,7 @@ class ExpertBatch(Workload):
     def __init__(self, n_up=48, n_down=48):
         self.n_up, self.n_down = n_up, n_down
         self.name = "c4"
+        self.sustained = True
         self.desc = (f"Muon batch: {n_up} x 7168x2048 + {n_down} x 2048x7168 fp32, 5 NS steps "
                      "(bf16 operands, fp32 accumulation)")
         ns = ns_flops_per_iter(2048, 7168)
@@ -218,6 +237,11 @@ class ExpertBatch(Workload):
 
     def make(self, device):
         return mc_inputs.c4(device=device, n_up=self.n_up, n_down=self.n_down)
+
+    def cpu_state(self):
+        """The oracle sample reads one up-projection's momentum: draw the
+        recipe with that one matrix instead of all 96 (17 GB on the host)."""
+        return mc_inputs.c4(device="cpu", n_up=1, n_down=0)
 
     def inputs(self, s):
         return s["grad"]
@@ -253,6 +277,7 @@ class MlaLayer(Workload):
         self.B = B if B is not None else (1 if which == "c5" else 16)
         self.T = T if T is not None else (32768 if which == "c5" else 4096)
         self.muon = which == "c5"
+        self.sustained = True
         self.desc = (f"K2-shaped MLA layer bf16 x[{self.B},{self.T},7168] H=64 q_lora 1536 "
                      f"kv_lora 512 nope 128 rope 64 causal"
                      + ("; Muon on W_qa, W_qb, W_kva, W_kb; MLA clip" if self.muon else ""))
@@ -480,13 +505,19 @@ def job_tflops(world: int, flops_per_rank: float, seconds: float) -> float:
     return world * flops_per_rank / seconds / 1e12
 
 
+def line_config(wl, world: int) -> dict:
+    """The workload description both arms print in ``config``."""
+    return {"workload": wl.desc, "l2": "flushed between timed steps (256 MiB write)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
 def run_reference(args, wl):
     """The fp64 oracle on the host cores: each step is one bounded sample of
     the workload (inputs drawn on the CPU)."""
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    s = wl.make("cpu")
+    s = wl.cpu_state() if hasattr(wl, "cpu_state") else wl.make("cpu")
     for _ in range(min(args.warmup, 1)):
         wl.oracle_sample(s)
     times, flops, sample = [], 0, ""
@@ -501,7 +532,7 @@ def run_reference(args, wl):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * tot / len(times), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.desc, "sample": sample},
+            "config": line_config(wl, world),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -509,29 +540,46 @@ def run_reference(args, wl):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, wl):
+def roofline_entry(wl, name, trace, K, peaks) -> dict:
+    """Roofline of kernel kind ``name``: its algorithmic work per launch over
+    its mean event-timed launch duration, against the measured peak."""
+    hbm_peak, bf16_peak, bf16_sus, peak_src = peaks
+    kind, work = wl.units[name]
+    n_launch = trace[name][0] / K
+    dur = trace[name][1] / trace[name][0] * 1e-3      # s per launch
+    if kind == "tensor":
+        achieved = work / n_launch / dur / 1e12
+        sus = wl.sustained and bf16_sus is not None
+        peak = bf16_sus if sus else bf16_peak
+        return {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "frac_of_burst_peak": achieved / bf16_peak,
+                "traffic": TRAFFIC.get((wl.name, name)),
+                "peak_kind": f"{peak_src} bf16 dense ({'sustained' if sus else 'burst'})"}
+    achieved = work / n_launch / dur / 1e9
+    return {"kernel": name, "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
+            "unit": "GB/s", "frac": achieved / hbm_peak,
+            "traffic": TRAFFIC.get((wl.name, name)),
+            "peak_kind": f"{peak_src} HBM copy"}
+
+
+def measure(wl, args, api, device, world, flush, e2e: bool = True) -> dict:
+    """Everything the line reports for workload ``wl`` on this rank: the
+    device time per step (whole step as one CUDA graph, L2 flushed between
+    timed steps), the scan and Muon halves alone, per-kernel event times, the
+    dominant kernel's roofline and, if ``e2e``, the end-to-end rate through
+    the public API with host copies inside the timed region."""
     import torch
-    import torch.distributed as dist
+    from muonclip_mc_max_gb300.step import CapturedStep
 
-    world, rank, local = dist_env()
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    if world > 1:
-        dist.init_process_group("nccl")
-
-    from muonclip_mc_max_gb300 import api, build
-    build.build()
-    api.load_library()
     s = wl.make(device)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream()
 
     def barrier():
         torch.cuda.synchronize()
         if world > 1:
+            import torch.distributed as dist
             dist.barrier()
-
-    from muonclip_mc_max_gb300.step import CapturedStep
 
     # the whole step as one CUDA graph (launch-bound at small sizes); the
     # scan and Muon halves are also captured alone for the breakdown
@@ -548,7 +596,7 @@ def run_ours(args, wl):
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(device.index or 0)
     clocks.start()
     barrier()
     for k in range(K):
@@ -559,13 +607,11 @@ def run_ours(args, wl):
     barrier()
     clk = clocks.stop()
     clip = clip_summary(s)  # the last timed step's S_max and gamma
-    launches = per_step_launches * K
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    tot_ms = max_over_ranks(sum(step_ms), world, device)
-    ms = tot_ms / K
+    ms = max_over_ranks(sum(step_ms), world, device) / K
     flops = wl.scan_flops + wl.ns_flops
-    value = job_tflops(world, flops, ms * 1e-3)
-    hbm_peak, bf16_peak, bf16_sus, peak_src = load_peaks()
+    peaks = load_peaks()
+    bf16_peak = peaks[1]
 
     def part_ms(g):
         if g is None:
@@ -611,22 +657,23 @@ def run_ours(args, wl):
                 entry["achieved_gbs"] = work / (tms / K * 1e-3) / 1e9
         kernels[name] = entry
     dominant = max((k for k in kernels if k in wl.units), key=lambda k: trace[k][1])
-    kind, work = wl.units[dominant]
-    n_launch = trace[dominant][0] / K
-    dur = trace[dominant][1] / trace[dominant][0] * 1e-3      # s per launch
-    if kind == "tensor":
-        achieved = work / n_launch / dur / 1e12
-        roof = {"kernel": dominant, "bound": "tensor", "achieved": achieved, "peak": bf16_peak,
-                "unit": "TFLOP/s", "frac": achieved / bf16_peak,
-                "traffic": TRAFFIC.get((wl.name, dominant)),
-                "peak_kind": f"{peak_src} bf16 dense (burst)"}
-    else:
-        achieved = work / n_launch / dur / 1e9
-        roof = {"kernel": dominant, "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
-                "unit": "GB/s", "frac": achieved / hbm_peak,
-                "traffic": TRAFFIC.get((wl.name, dominant)),
-                "peak_kind": f"{peak_src} HBM copy"}
+    roof = roofline_entry(wl, dominant, trace, K, peaks)
+    # every HBM-bound pass gets its own entry too
+    hbm_roofs = {k: roofline_entry(wl, k, trace, K, peaks) for k in kernels
+                 if k in wl.units and wl.units[k][0] == "hbm"}
     assert api.mc_read_device_status(clear=True) == 0, "device status set during timing"
+    del traced, g_scan, g_muon
+
+    res = {"wl": wl, "ms": ms, "value": job_tflops(world, flops, ms * 1e-3), "clk": clk,
+           "clip": clip, "launches": per_step_launches * K, "scan_ms": scan_t, "muon_ms": muon_t,
+           "scan_tflops": (wl.scan_flops / (scan_t * 1e-3) / 1e12) if scan_t else None,
+           "ns_tflops": (wl.ns_flops / (muon_t * 1e-3) / 1e12) if muon_t else None,
+           "roof": roof, "hbm_roofs": hbm_roofs, "kernels": kernels, "state": s}
+    res["scan_frac_bf16_peak"] = res["scan_tflops"] / bf16_peak if scan_t else None
+    res["ns_frac_bf16_peak"] = res["ns_tflops"] / bf16_peak if muon_t else None
+    if not e2e:
+        del graph
+        return res
 
     # ---- end to end through the public API: every step uploads its inputs
     # from pinned host memory and reads its results back.  Two input buffer
@@ -673,45 +720,82 @@ def run_ours(args, wl):
     copy_stream.synchronize()
     barrier()
     e2e_s = max_over_ranks(time.perf_counter() - t0, world, device)
-    e2e_value = job_tflops(world, flops * K, e2e_s)
+    res["e2e"] = {"value": job_tflops(world, flops * K, e2e_s), "unit": "TFLOP/s",
+                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    del graph, graph_twin, graphs, s_twin, ins_sets, outs_sets, host_in, host_out
+    return res
 
-    line = None
+
+def cpu_baseline(wl, s) -> dict:
+    """The oracle on this host's cores, repeated for about 10 s of CPU work."""
+    f_tot, dt_tot, sample, reps = 0, 0.0, "", 0
+    while dt_tot < 10.0 and reps < 50:
+        f, dt, sample = wl.oracle_sample(s)
+        f_tot += f
+        dt_tot += dt
+        reps += 1
+    return {"value": f_tot / dt_tot / 1e12, "unit": "TFLOP/s",
+            "cores": int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)),
+            "kind": "oracle", "sample": f"{sample}; {reps} repetitions, {dt_tot:.1f} s"}
+
+
+def run_ours(args, wl, extra=None):
+    """Times ``wl`` (the line's headline) and, if given, ``extra`` (the long
+    MLA MuonClip step, reported beside it) on this rank."""
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl")
+
+    from muonclip_mc_max_gb300 import api, build
+    build.build()
+    api.load_library()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    K = args.steps
+
+    r = measure(wl, args, api, device, world, flush, e2e=True)
+    cpu = cpu_baseline(wl, r["state"]) if rank == 0 else None
+    r.pop("state")
+    torch.cuda.empty_cache()
+    rx = None
+    if extra is not None:
+        rx = measure(extra, args, api, device, world, flush, e2e=False)
+        rx.pop("state")
+        torch.cuda.empty_cache()
+
     if rank == 0:
-        # the oracle on this host's cores, repeated for about 10 s of CPU work
-        f_tot, dt_tot, sample, reps = 0, 0.0, "", 0
-        while dt_tot < 10.0 and reps < 50:
-            f, dt, sample = wl.oracle_sample(s)
-            f_tot += f
-            dt_tot += dt
-            reps += 1
-        cpu = {"value": f_tot / dt_tot / 1e12, "unit": "TFLOP/s",
-               "cores": int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)),
-               "kind": "oracle", "sample": f"{sample}; {reps} repetitions, {dt_tot:.1f} s"}
         line = {
-            "metric": getattr(wl, "metric", METRIC), "value": value, "unit": "TFLOP/s", "n_gpus": world,
-            "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": ms,
+            "metric": getattr(wl, "metric", METRIC), "value": r["value"], "unit": "TFLOP/s",
+            "n_gpus": world, "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": r["ms"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16/fp16",
-            "data": "synthetic",
-            "config": {"workload": wl.desc, "l2": "flushed between timed steps (256 MiB write)",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-            "muonclip_step_ms": ms,
-            "scan_tflops": (wl.scan_flops / (scan_t * 1e-3) / 1e12) if scan_t else None,
-            "scan_frac_bf16_peak": ((wl.scan_flops / (scan_t * 1e-3) / 1e12) / bf16_peak)
-            if scan_t else None,
-            "ns_tflops": (wl.ns_flops / (muon_t * 1e-3) / 1e12) if muon_t else None,
-            "ns_frac_bf16_peak": ((wl.ns_flops / (muon_t * 1e-3) / 1e12) / bf16_peak)
-            if muon_t else None,
-            "scan_ms": scan_t, "muon_ms": muon_t,
-            "roofline": roof,
-            "kernels": kernels,
-            "gpu_launches": int(launches),
-            "clocks": clk,
-            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+            "data": "synthetic", "config": line_config(wl, world),
+            "muonclip_step_ms": r["ms"] if r["scan_ms"] is not None else None,
+            "scan_tflops": r["scan_tflops"], "scan_frac_bf16_peak": r["scan_frac_bf16_peak"],
+            "ns_tflops": r["ns_tflops"], "ns_frac_bf16_peak": r["ns_frac_bf16_peak"],
+            "scan_ms": r["scan_ms"], "muon_ms": r["muon_ms"],
+            "roofline": r["roof"], "hbm_passes": r["hbm_roofs"], "kernels": r["kernels"],
+            "gpu_launches": int(r["launches"]), "clocks": r["clk"], "e2e": r["e2e"],
             "cpu_baseline": cpu,
         }
-        if clip is not None:
-            line["clip"] = clip
+        if r["clip"] is not None:
+            line["clip"] = r["clip"]
+        if rx is not None:
+            xw = rx["wl"]
+            line["muonclip_step_ms"] = rx["ms"]
+            line["scan_tflops"] = rx["scan_tflops"]
+            line["scan_frac_bf16_peak"] = rx["scan_frac_bf16_peak"]
+            line["scan_ms"] = rx["scan_ms"]
+            line["long_mla"] = {
+                "workload": xw.desc, "muonclip_step_ms": rx["ms"], "value": rx["value"],
+                "unit": "TFLOP/s", "scan_tflops": rx["scan_tflops"],
+                "scan_frac_bf16_peak": rx["scan_frac_bf16_peak"], "scan_ms": rx["scan_ms"],
+                "ns_tflops": rx["ns_tflops"], "muon_ms": rx["muon_ms"],
+                "roofline": rx["roof"], "kernels": rx["kernels"], "clip": rx["clip"],
+                "gpu_launches": int(rx["launches"]), "clocks": rx["clk"]}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
@@ -721,17 +805,22 @@ def run_ours(args, wl):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c2")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c4")
     ap.add_argument("--experts", type=int, default=48,
                     help="c4: up- and down-projections each (smaller for profiling)")
     ap.add_argument("--seqs", type=int, default=None, help="c3/c5: sequences (smaller for profiling)")
     ap.add_argument("--tokens", type=int, default=None, help="c3/c5: tokens per sequence")
+    ap.add_argument("--no-long-mla", action="store_true",
+                    help="c4: leave out the long-context MLA MuonClip step reported beside it")
     args = ap.parse_args()
+    extra = None
     if args.workload == "c4":
         wl = ExpertBatch(args.experts, args.experts)
+        if not args.no_long_mla:
+            extra = MlaLayer("c5", B=args.seqs, T=args.tokens)
     elif args.workload in ("c3", "c5"):
         wl = MlaLayer(args.workload, B=args.seqs, T=args.tokens)
     else:
@@ -739,7 +828,7 @@ def main():
     if args.impl == "reference":
         run_reference(args, wl)
     else:
-        run_ours(args, wl)
+        run_ours(args, wl, extra)
 
 
 if __name__ == "__main__":

@@ -19,6 +19,8 @@
  *   - Every data pointer is DEVICE memory owned by the caller.  The library
  *     never allocates or frees device memory; scratch comes from the
  *     caller's workspace, sized by the matching *_workspace_size call.
+ *     A *_workspace_size call returns SIZE_MAX for sizes whose scratch does
+ *     not fit in size_t; no workspace can then pass the entry point's check.
  *     Arrays of pointers (mc_muon_step, mc_newton_schulz) are HOST arrays
  *     holding device pointers; they are read before the call returns.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
@@ -113,7 +115,9 @@ mc_status mc_max_logits_mha(const void* x, const void* wq, const void* wk, mc_dt
  * graph, where cudaMalloc is not allowed.  Such a caller cannot hand over a
  * workspace, so this entry point uses scratch that lives in the library:
  * one static device array of MC_NOALLOC_SCRATCH_BYTES, which every GPU that
- * loads the library holds until the process exits.
+ * loads the library holds until the process exits.  The array belongs to
+ * the library's device module, so a device holds it as soon as any entry
+ * point of the library has run there, not only after calls of this one.
  *
  * Same arguments, results and errors as mc_max_logits_mha, without ws and
  * ws_bytes.  Sizes whose scratch (mc_max_logits_mha_workspace_size) exceeds

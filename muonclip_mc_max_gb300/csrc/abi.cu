@@ -1,6 +1,11 @@
 // abi.cu -- the C ABI of include/mc_max.h: argument checks, workspace
 // carving, tensor-map encoding and launch sequencing on the caller's stream.
-// No device memory is allocated here; every buffer is the caller's.
+// Nothing here allocates device memory at run time; every buffer is the
+// caller's.  The library's only device storage is static and part of its
+// device module: the 4-byte status word and the 64 MiB scratch array of
+// mc_max_logits_mha_noalloc.  The module is loaded on a device the first
+// time any entry point runs there, so every device where the library has
+// run holds both until the process exits.
 #include <algorithm>
 #include <atomic>
 #include <map>
@@ -191,11 +196,23 @@ TraceScope::~TraceScope() {
 static size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
 // bump allocator over the caller's workspace
+// a * b, or SIZE_MAX when the product does not fit size_t
+static size_t mul_sat(size_t a, size_t b) { return (a && b > SIZE_MAX / a) ? SIZE_MAX : a * b; }
+static size_t mul_sat(size_t a, size_t b, size_t c) { return mul_sat(mul_sat(a, b), c); }
+
+// Carves 256-byte-aligned pieces out of a workspace (or, with base null,
+// only sums their sizes).  The sum saturates at SIZE_MAX instead of
+// wrapping, so a size that does not fit size_t can never pass a workspace
+// check; callers compare ``used`` against the workspace before carving.
 struct Carve {
     uint8_t* base;
     size_t used;
     template <typename T>
     T* take(size_t count) {
+        if (used > SIZE_MAX - 512 || count > (SIZE_MAX - 512 - used) / sizeof(T)) {
+            used = SIZE_MAX;
+            return nullptr;
+        }
         T* p = base ? reinterpret_cast<T*>(base + used) : nullptr;
         used += align256(count * sizeof(T));
         return p;
@@ -328,7 +345,7 @@ static bool mha_tensor_path(mc_dtype dt, int D, int dh) { return dt == MC_BF16 &
 
 static size_t mha_carve(Carve& c, int B, int T, int D, int H, int dh, mc_dtype dt, void** q, void** k,
                         unsigned** keys) {
-    size_t n = (size_t)B * T * H * dh;
+    const size_t n = mul_sat((size_t)B * T, (size_t)H * dh);
     if (mha_tensor_path(dt, D, dh)) {
         *q = c.take<__half>(n);
         *k = c.take<__half>(n);
@@ -468,6 +485,7 @@ mc_status mc_max_logits_mha_noalloc(const void* x, const void* wq, const void* w
                                     int D, int H, int dh, int causal, int accumulate, float* s_max,
                                     float* s_max_bh, mc_stream_t stream) {
     if (B <= 0 || T <= 0 || D <= 0 || H <= 0 || dh <= 0) return MC_ERR_INVALID_ARG;
+    if ((int64_t)B * T > INT32_MAX || (int64_t)H * dh > INT32_MAX) return MC_ERR_UNSUPPORTED;
     if (mc_max_logits_mha_workspace_size(B, T, D, H, dh, dtype) > MC_NOALLOC_SCRATCH_BYTES) return MC_ERR_WORKSPACE;
     void* scratch = noalloc_scratch();
     if (!scratch) return MC_ERR_CUDA;
@@ -499,13 +517,14 @@ struct MlaWs {
 static size_t mla_carve(Carve& c, const mc_mla_layer* L, int B, int T, MlaWs& w) {
     size_t BT = (size_t)B * T;
     w.rope = c.take<float2>((size_t)T * 32);
-    w.cq = c.take<__half>(BT * L->q_lora);
-    w.ckv = c.take<__half>(BT * (L->kv_lora + L->rope));
-    w.q = c.take<__half>(BT * (size_t)L->H * (L->nope + L->rope));
-    w.kc = c.take<__half>(BT * (size_t)L->H * L->nope);
-    w.wqb = c.take<__half>((size_t)L->q_lora * L->H * (L->nope + L->rope));
-    w.wkb = c.take<__half>((size_t)L->kv_lora * L->H * L->nope);
-    w.keys = c.take<unsigned>((size_t)B * L->H + 1);  // + the scan's done-counter
+    const size_t H = (size_t)L->H, qk = (size_t)L->nope + L->rope;
+    w.cq = c.take<__half>(mul_sat(BT, L->q_lora));
+    w.ckv = c.take<__half>(mul_sat(BT, (size_t)L->kv_lora + L->rope));
+    w.q = c.take<__half>(mul_sat(BT, H, qk));
+    w.kc = c.take<__half>(mul_sat(BT, H, L->nope));
+    w.wqb = c.take<__half>(mul_sat(L->q_lora, H, qk));
+    w.wkb = c.take<__half>(mul_sat(L->kv_lora, H, L->nope));
+    w.keys = c.take<unsigned>((size_t)B * H + 1);  // + the scan's done-counter
     return c.used;
 }
 
@@ -714,10 +733,10 @@ bool plan_ns(const int* rows, const int* cols, int count, uint8_t* base, NsPlan&
         g.zbase = (int)P.order.size();
         for (int i : g.idx) P.order.push_back(i);
         size_t cnt = g.idx.size();
-        g.X[0] = c.take<__nv_bfloat16>(cnt * g.m_pad * g.n_pad);
-        g.X[1] = c.take<__nv_bfloat16>(cnt * g.m_pad * g.n_pad);
-        g.A = c.take<__nv_bfloat16>(cnt * g.m_pad * g.m_pad);
-        g.Bm = c.take<__nv_bfloat16>(cnt * g.m_pad * g.m_pad);
+        g.X[0] = c.take<__nv_bfloat16>(mul_sat(cnt, g.m_pad, g.n_pad));
+        g.X[1] = c.take<__nv_bfloat16>(mul_sat(cnt, g.m_pad, g.n_pad));
+        g.A = c.take<__nv_bfloat16>(mul_sat(cnt, g.m_pad, g.m_pad));
+        g.Bm = c.take<__nv_bfloat16>(mul_sat(cnt, g.m_pad, g.m_pad));
     }
     P.part.assign(count, nullptr);
     P.nparts.assign(count, 0);
@@ -739,6 +758,7 @@ bool valid_mats(const int* rows, const int* cols, int count) {
     if (!rows || !cols || count <= 0) return false;
     for (int i = 0; i < count; ++i) {
         if (rows[i] <= 0 || cols[i] <= 0) return false;
+        if (rows[i] > (1 << 30) || cols[i] > (1 << 30)) return false;  // padded sizes stay in int
         if ((int64_t)rows[i] * cols[i] > ((int64_t)1 << 31)) return false;
     }
     return true;

@@ -106,3 +106,17 @@ def test_workspace_sizes(lib):
     c = api.mc_max_logits_mla_workspace_size(L, 16, 4096)
     # c_Q, [c_KV|k^R], [q^C|q^R] and k^C of a K2-shaped layer at B=16, T=4096
     assert c >= 65536 * (1536 + 576 + 64 * 192 + 64 * 128) * 2
+
+
+def test_workspace_sizes_saturate_instead_of_wrapping(lib):
+    """Sizes whose scratch does not fit size_t report SIZE_MAX, so no
+    workspace (nor the allocation-free scratch) can pass the size check;
+    the largest int sizes give B*T*H*dh near 2^62 elements."""
+    big = 2 ** 31 - 1
+    size_max = 2 ** 64 - 1
+    for dt in (api.MC_BF16, api.MC_F32):
+        assert api.mc_max_logits_mha_workspace_size(65535, 32767, 64, 32767, 65535, dt) == size_max
+    assert api.mc_max_logits_mha_workspace_size(1, big, 64, 1, 64, api.MC_BF16) < size_max
+    L = api.MlaLayer(D=7168, q_lora=big, kv_lora=big, H=big, nope=128, rope=64, rope_base=5e4,
+                     wtype=1)
+    assert api.mc_max_logits_mla_workspace_size(L, big, big) == size_max

@@ -118,7 +118,7 @@ def test_reference_arm_prints_one_contract_line():
                 "cpu_baseline", "e2e", "impl"):
         assert key in line, key
     assert line["impl"] == "reference" and line["value"] > 0 and line["steps"] == 1
-    assert line["config"]["workload"].startswith("MHA layer")
+    assert line["config"]["workload"].startswith("Muon batch: 48 x 7168x2048")
     assert line["cpu_baseline"]["value"] == line["value"]
 
 

@@ -3,13 +3,16 @@ times: the CUDA path runs the whole workload, the fp64 oracle (its
 library-GEMM restatement) recomputes sampled outputs one by one, and
 properties that hold at any size cover the rest.
 
-  MHA layer   x [8,1024,1024], 16 heads of 64: S_max of sampled (sequence,
-              head) pairs, gamma and the clip bit-exact, both Muon matrices.
-  K2 MLA      x [16,4096,7168] causal: sampled (sequence, head) pairs.
+  MHA layer   x [8,1024,1024], 16 heads of 64: S_max of every head of two
+              sequences and one rotating head of each other sequence, gamma
+              and the clip bit-exact, both Muon matrices.
+  K2 MLA      x [16,4096,7168] causal: every head of two sequences and one
+              rotating head of each of the other 14.
   expert batch 96 matrices of 7168x2048 / 2048x7168: two matrices against
               the oracle, every matrix's momentum and update RMS checked.
-  long MLA    x [1,32768,7168] causal + heavy rows: sampled heads, the MLA
-              clip bit-exact, Muon on W_kva and W_kb against the oracle.
+  long MLA    x [1,32768,7168] causal + heavy rows: the 8 planted heads and
+              8 cold ones, the MLA clip bit-exact, Muon on W_kva and W_kb
+              against the oracle.
 """
 import gc
 
@@ -46,12 +49,16 @@ def test_mha_layer_fullsize():
     s_bh = torch.empty(B, H, dtype=torch.float32, device=dev())
     s = api.mc_max_logits_mha(x, wq, wk, H, dh, s_max_bh=s_bh)
     torch.cuda.synchronize()
-    cold = [h for h in range(H) if h not in inp["hot"]][:2]
-    heads = inp["hot"] + cold
-    ref = oracle.max_logits_mha_np(x.cpu(), wq.cpu(), wk.cpu(), H, dh, False, heads=heads,
-                                   batches=[0, 7])
-    got = s_bh.cpu().numpy()[[0, 7]][:, heads]
+    # every head of two sequences (the first and the last scheduling band)
+    ref = oracle.max_logits_mha_np(x.cpu(), wq.cpu(), wk.cpu(), H, dh, False, batches=[0, 7])
+    got = s_bh.cpu().numpy()[[0, 7]]
     assert rel_err(got, ref).max() < SMAX_RTOL
+    # and one head of every other sequence, rotating through the heads
+    for b in range(1, 7):
+        h = (5 * b) % H
+        ref = oracle.max_logits_mha_np(x.cpu(), wq.cpu(), wk.cpu(), H, dh, False, heads=[h],
+                                       batches=[b])
+        assert rel_err(s_bh.cpu().numpy()[b, h], ref[0, 0]) < SMAX_RTOL, (b, h)
     assert np.array_equal(s.cpu().numpy(), s_bh.cpu().numpy().max(0))
     # Muon on both 1024 x 1024 masters
     w0 = [t.cpu() for t in inp["w_master"]]
@@ -88,14 +95,19 @@ def test_k2_mla_layer_fullsize():
     api.mc_max_logits_mla(d["x"], d["w_qa"], d["w_qb"], d["w_kva"], d["w_kb"], H, 128, 64,
                           inp["rope_base"], causal=True, s_max_bh=s_bh)
     torch.cuda.synchronize()
-    cold = [h for h in range(H) if h not in inp["hot"]][:2]
-    heads = inp["hot"][:2] + cold
-    b = 5
-    ref = oracle.max_logits_mla_np(d["x"][b:b + 1].cpu(), d["w_qa"].cpu(), d["w_qb"].cpu(),
-                                   d["w_kva"].cpu(), d["w_kb"].cpu(), H, 128, 64,
-                                   inp["rope_base"], True, heads=heads)
-    got = s_bh.cpu().numpy()[b:b + 1][:, heads]
-    assert rel_err(got, ref).max() < SMAX_RTOL, (got, ref)
+    got_all = s_bh.cpu().numpy()
+    w = [d[k].cpu() for k in ("w_qa", "w_qb", "w_kva", "w_kb")]
+    x_cpu = d["x"].cpu()
+    # every head of two sequences (first and last scheduling band)
+    for b in (0, 15):
+        ref = oracle.max_logits_mla_np(x_cpu[b:b + 1], *w, H, 128, 64, inp["rope_base"], True)
+        assert rel_err(got_all[b:b + 1], ref).max() < SMAX_RTOL, b
+    # one head of every other sequence, rotating through the heads (hot ones included)
+    for b in range(1, 15):
+        h = inp["hot"][b % len(inp["hot"])] if b % 4 == 0 else (9 * b + 1) % H
+        ref = oracle.max_logits_mla_np(x_cpu[b:b + 1], *w, H, 128, 64, inp["rope_base"], True,
+                                       heads=[h])
+        assert rel_err(got_all[b, h], ref[0, 0]) < SMAX_RTOL, (b, h)
     assert api.mc_read_device_status(clear=True) == 0
     del inp, d, s_bh
     _free()
@@ -144,8 +156,10 @@ def test_long_mla_fullsize():
     s = api.mc_max_logits_mla(d["x"], d["w_qa"], d["w_qb"], d["w_kva"], d["w_kb"], H, 128, 64,
                               inp["rope_base"], causal=True, s_max_bh=s_bh)
     torch.cuda.synchronize()
-    cold = [h for h in range(H) if h not in inp["hot"]][:1]
-    heads = inp["hot"][:2] + cold
+    # all 8 planted heads and 8 cold ones spread over the head range
+    cold = [h for h in range(H) if h not in inp["hot"]][::7][:8]
+    heads = inp["hot"] + cold
+    assert len(heads) == 16
     ref = oracle.max_logits_mla_np(d["x"].cpu(), d["w_qa"].cpu(), d["w_qb"].cpu(),
                                    d["w_kva"].cpu(), d["w_kb"].cpu(), H, 128, 64,
                                    inp["rope_base"], True, heads=heads)
