@@ -281,6 +281,53 @@ mc_status mc_muon_step(float* const* w, const float* const* g, float* const* m, 
                        void* ws, size_t ws_bytes, mc_stream_t stream);
 
 /* ======================================================================
+ * (4) Data-parallel exchange: Distributed Muon and the S_max max over ranks
+ *
+ * "Notes on Moonlight", section "Distributed Muon": under ZeRO-1 every
+ * data-parallel rank holds one partition of each matrix's optimizer state;
+ * Muon adds a DP gather of the partitions into the full matrix and a full
+ * Newton-Schulz update on it.  Here a partition is a block of whole rows,
+ * so momentum, the update and QK-Clip run on it unchanged; the collectives
+ * themselves belong to the caller (NCCL through torch.distributed in the
+ * binding).  The per-head max logit is a max over every X in the global
+ * batch (Kimi K2 section 2.1, S_max equation): each rank scans its own
+ * micro-batch and the ranks' results are combined by one all-reduce(MAX).
+ * ====================================================================== */
+
+/*
+ * Order-preserving int32 keys of fp32 S_max values, for that all-reduce:
+ * a < b implies key(a) < key(b), -0 sits just below +0, and every NaN maps
+ * to INT32_MAX, so a NaN max logit on any rank reaches every rank (a float
+ * max reduction may drop NaN).  mc_smax_from_keys inverts the map (any NaN
+ * comes back as a quiet NaN).  s_max, keys: device arrays of n entries.
+ */
+mc_status mc_smax_to_keys(const float* s_max, int* keys, int n, mc_stream_t stream);
+mc_status mc_smax_from_keys(const int* keys, float* s_max, int n, mc_stream_t stream);
+
+/*
+ * Momentum on one shard of n elements ("Notes on Moonlight", "Background"):
+ *   m <- mu m + grad_scale g      (grad_scale = 1/world turns a summed
+ *                                  reduce-scatter into the mean gradient)
+ *   u  = m, or grad_scale g + mu m when nesterov != 0   (u may be NULL when
+ *        nesterov == 0; it is the shard sent to the matrix's owner)
+ * m, g, u: device f32, 4-byte aligned; u may not alias m or g.  The same
+ * fused multiply-adds as mc_muon_step's momentum, element for element.
+ */
+mc_status mc_muon_momentum(float* m, const float* g, float* u, size_t n, float mu,
+                           float grad_scale, int nesterov, mc_stream_t stream);
+
+/*
+ * Update of one shard of n elements with the owner's Newton-Schulz output
+ * ("Notes on Moonlight", "Scaling up Muon"):
+ *   w <- w - lr (rms_coef sqrt(max(rows, cols)) o + wd w)
+ * rows, cols: the FULL matrix (they set the RMS scale); w, o: device f32,
+ * 4-byte aligned, not aliased.  Rounds exactly as mc_muon_step's update,
+ * so a sharded step equals the whole-matrix step bit for bit.
+ */
+mc_status mc_muon_apply(float* w, const float* o, size_t n, int rows, int cols, float lr,
+                        float rms_coef, float wd, mc_stream_t stream);
+
+/* ======================================================================
  * Tensor-core GEMM (the contraction core the three parts share)
  * ====================================================================== */
 

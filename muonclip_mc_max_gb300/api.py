@@ -25,6 +25,7 @@ __all__ = [
     "mc_qk_clip_mha", "mc_qk_clip_mla", "mc_qk_clip_global",
     "mc_newton_schulz", "mc_newton_schulz_workspace_size",
     "mc_muon_step", "mc_muon_workspace_size", "mc_gemm_bf16",
+    "mc_smax_to_keys", "mc_smax_from_keys", "mc_muon_momentum", "mc_muon_apply",
     "mc_launch_count", "mc_trace_enable", "mc_trace_collect", "mc_selftest_wait_timeout",
     "MC_F32", "MC_BF16", "MC_DEV_NONFINITE", "MC_DEV_TIMEOUT", "MC_DEV_RANGE", "NS_COEFFS",
 ]
@@ -98,6 +99,10 @@ def load_library():
         "mc_newton_schulz": ([VP, VP, IP, IP, I, I, F, F, F, F, V, S, V], I),
         "mc_muon_step": ([VP, VP, VP, IP, IP, I, F, F, F, F, I, F, F, F, F, I, V, S, V], I),
         "mc_gemm_bf16": ([V, V, V, I, I, I, I, I, I, V], I),
+        "mc_smax_to_keys": ([V, V, I, V], I),
+        "mc_smax_from_keys": ([V, V, I, V], I),
+        "mc_muon_momentum": ([V, V, V, S, F, F, I, V], I),
+        "mc_muon_apply": ([V, V, S, I, I, F, F, F, V], I),
         "mc_selftest_wait_timeout": ([U, V, V], I),
         "mc_launch_count": ([], ctypes.c_ulonglong),
         "mc_trace_enable": ([I], I),
@@ -393,6 +398,66 @@ def mc_muon_step(w, g, m, lr: float, mu: float = 0.95, wd: float = 0.1, rms: flo
     _check("mc_muon_step", lib.mc_muon_step(
         _ptrs(w), _ptrs(g), _ptrs(m), rows, cols, n, lr, mu, wd, rms, steps, a, b, c, eps,
         int(nesterov), ws, nb, _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# (4) data-parallel exchange helpers
+# ---------------------------------------------------------------------------
+
+def mc_smax_to_keys(s_max, keys=None, stream=None):
+    """f32 S_max [n] -> order-preserving int32 keys [n] (NaN largest)."""
+    lib = load_library()
+    _need_cuda(s_max, keys)
+    if s_max.dtype != torch.float32:
+        raise ValueError("s_max must be float32")
+    if keys is None:
+        keys = torch.empty(s_max.shape, dtype=torch.int32, device=s_max.device)
+    elif keys.dtype != torch.int32 or keys.numel() != s_max.numel():
+        raise ValueError("keys must be int32 with one entry per head")
+    _check("mc_smax_to_keys", lib.mc_smax_to_keys(_ptr(s_max), _ptr(keys), s_max.numel(),
+                                                  _stream(stream)))
+    return keys
+
+
+def mc_smax_from_keys(keys, s_max=None, stream=None):
+    """int32 keys [n] -> f32 S_max [n] (the inverse of mc_smax_to_keys)."""
+    lib = load_library()
+    _need_cuda(keys, s_max)
+    if keys.dtype != torch.int32:
+        raise ValueError("keys must be int32")
+    if s_max is None:
+        s_max = torch.empty(keys.shape, dtype=torch.float32, device=keys.device)
+    elif s_max.dtype != torch.float32 or s_max.numel() != keys.numel():
+        raise ValueError("s_max must be float32 with one entry per key")
+    _check("mc_smax_from_keys", lib.mc_smax_from_keys(_ptr(keys), _ptr(s_max), keys.numel(),
+                                                      _stream(stream)))
+    return s_max
+
+
+def mc_muon_momentum(m, g, u=None, mu: float = 0.95, grad_scale: float = 1.0,
+                     nesterov: bool = False, stream=None):
+    """In-place m <- mu m + grad_scale g on one f32 shard; u (optional, same
+    size) receives the Newton-Schulz input (m, or the Nesterov input)."""
+    lib = load_library()
+    _need_cuda(m, g, u)
+    for t in (m, g, u):
+        if t is not None and (t.dtype != torch.float32 or t.numel() != m.numel()):
+            raise ValueError("m, g, u must be float32 of equal size")
+    _check("mc_muon_momentum", lib.mc_muon_momentum(_ptr(m), _ptr(g), _ptr(u), m.numel(), mu,
+                                                    grad_scale, int(nesterov), _stream(stream)))
+    return u if u is not None else m
+
+
+def mc_muon_apply(w, o, rows: int, cols: int, lr: float, rms: float = 0.2, wd: float = 0.1,
+                  stream=None):
+    """In-place w <- w - lr (rms sqrt(max(rows, cols)) o + wd w) on one f32
+    shard of a [rows, cols] matrix."""
+    lib = load_library()
+    _need_cuda(w, o)
+    if w.dtype != torch.float32 or o.dtype != torch.float32 or o.numel() != w.numel():
+        raise ValueError("w and o must be float32 of equal size")
+    _check("mc_muon_apply", lib.mc_muon_apply(_ptr(w), _ptr(o), w.numel(), int(rows), int(cols),
+                                              lr, rms, wd, _stream(stream)))
 
 
 # ---------------------------------------------------------------------------

@@ -1045,6 +1045,47 @@ mc_status mc_muon_step(float* const* w, const float* const* g, float* const* m, 
 }
 
 // ===========================================================================
+// data-parallel exchange helpers (Distributed Muon, S_max over ranks)
+// ===========================================================================
+
+mc_status mc_smax_to_keys(const float* s_max, int* keys, int n, mc_stream_t stream) {
+    if (n < 0 || (n > 0 && (!s_max || !keys))) return MC_ERR_INVALID_ARG;
+    if (n > 0 && (!aligned4(s_max) || !aligned4(keys))) return MC_ERR_INVALID_ARG;
+    MC_CUDA(launch_smax_keys(s_max, keys, nullptr, nullptr, n, (cudaStream_t)stream));
+    return MC_OK;
+}
+
+mc_status mc_smax_from_keys(const int* keys, float* s_max, int n, mc_stream_t stream) {
+    if (n < 0 || (n > 0 && (!s_max || !keys))) return MC_ERR_INVALID_ARG;
+    if (n > 0 && (!aligned4(s_max) || !aligned4(keys))) return MC_ERR_INVALID_ARG;
+    MC_CUDA(launch_smax_keys(nullptr, nullptr, keys, s_max, n, (cudaStream_t)stream));
+    return MC_OK;
+}
+
+mc_status mc_muon_momentum(float* m, const float* g, float* u, size_t n, float mu, float grad_scale, int nesterov,
+                           mc_stream_t stream) {
+    if (n == 0) return MC_OK;
+    if (!m || !g || (nesterov && !u)) return MC_ERR_INVALID_ARG;
+    if (n > (size_t)INT64_MAX / 4) return MC_ERR_INVALID_ARG;
+    if (!aligned4(m) || !aligned4(g) || (u && !aligned4(u))) return MC_ERR_INVALID_ARG;
+    if ((const float*)m == g || u == m || (const float*)u == g) return MC_ERR_INVALID_ARG;
+    MC_CUDA(launch_momentum_flat(m, g, u, (long long)n, mu, grad_scale, nesterov ? 1 : 0, (cudaStream_t)stream));
+    return MC_OK;
+}
+
+mc_status mc_muon_apply(float* w, const float* o, size_t n, int rows, int cols, float lr, float rms_coef, float wd,
+                        mc_stream_t stream) {
+    if (n == 0) return MC_OK;
+    if (!w || !o || rows <= 0 || cols <= 0 || (const float*)w == o) return MC_ERR_INVALID_ARG;
+    if (n > (size_t)INT64_MAX / 4) return MC_ERR_INVALID_ARG;
+    if (!aligned4(w) || !aligned4(o)) return MC_ERR_INVALID_ARG;
+    // the RMS scale exactly as the whole-matrix update forms it
+    const float rms = rms_coef * sqrtf((float)std::max(rows, cols));
+    MC_CUDA(launch_update_flat(w, o, (long long)n, lr, rms, wd, (cudaStream_t)stream));
+    return MC_OK;
+}
+
+// ===========================================================================
 // tensor-core GEMM
 // ===========================================================================
 

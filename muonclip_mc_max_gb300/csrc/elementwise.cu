@@ -187,6 +187,15 @@ cudaError_t launch_bf16_to_f16(const void* src, void* dst, long long n, cudaStre
 // ---------------------------------------------------------------------------
 // Muon passes over 64 x 64 tiles of X (the Newton-Schulz orientation)
 // ---------------------------------------------------------------------------
+
+// W <- W - lr (rms O + wd W) ("Notes on Moonlight", "Scaling up Muon"),
+// every product and sum rounded once in the order written.  The tiled pass
+// and the flat pass over a ZeRO-1 shard share it, so a sharded update
+// matches the whole-matrix one bit for bit.
+MC_D float muon_update_elem(float w, float o, float lr, float rms, float wd) {
+    return __fsub_rn(w, __fmul_rn(lr, __fadd_rn(__fmul_rn(rms, o), __fmul_rn(wd, w))));
+}
+
 constexpr int kTile = 64;
 constexpr int kMatThreads = 256;
 
@@ -340,19 +349,17 @@ __global__ void __launch_bounds__(kMatThreads) mat_pass_kernel(const __grid_cons
                         for (int k = 0; k < 4; ++k) {
                             if (c + k >= d.cols) break;
                             if (B.mode == 2) {
-                                const float w = d.w[off + k];
-                                d.w[off + k] = w - B.lr * (d.rms * o[k] + B.wd * w);
+                                d.w[off + k] = muon_update_elem(d.w[off + k], o[k], B.lr, d.rms, B.wd);
                             } else {
                                 d.w[off + k] = o[k];
                             }
                         }
                     } else if (B.mode == 2) {
                         float4 w = *reinterpret_cast<const float4*>(d.w + off);
-                        // W - lr (rms O + wd W), each step rounded as written
-                        w.x = w.x - B.lr * (d.rms * o[0] + B.wd * w.x);
-                        w.y = w.y - B.lr * (d.rms * o[1] + B.wd * w.y);
-                        w.z = w.z - B.lr * (d.rms * o[2] + B.wd * w.z);
-                        w.w = w.w - B.lr * (d.rms * o[3] + B.wd * w.w);
+                        w.x = muon_update_elem(w.x, o[0], B.lr, d.rms, B.wd);
+                        w.y = muon_update_elem(w.y, o[1], B.lr, d.rms, B.wd);
+                        w.z = muon_update_elem(w.z, o[2], B.lr, d.rms, B.wd);
+                        w.w = muon_update_elem(w.w, o[3], B.lr, d.rms, B.wd);
                         *reinterpret_cast<float4*>(d.w + off) = w;
                     } else {
                         *reinterpret_cast<float4*>(d.w + off) = make_float4(o[0], o[1], o[2], o[3]);
@@ -372,6 +379,121 @@ cudaError_t launch_mat_pass(const MatBatch& b, cudaStream_t stream) {
     static const char* names[4] = {"muon_momentum", "ns_cast", "muon_update", "ns_out"};
     TraceScope ts(names[b.mode & 3], stream);
     return launch_pdl(mat_pass_kernel, dim3(grid), dim3(kMatThreads), 0, stream, b);
+}
+
+// ---------------------------------------------------------------------------
+// Flat passes over one ZeRO-1 shard of a matrix ("Notes on Moonlight",
+// "Distributed Muon": the optimizer state is partitioned across the
+// data-parallel ranks; momentum and the update are elementwise, so each rank
+// applies them to its own block).  Same arithmetic as the tiled passes:
+//   momentum  M <- mu M + s G   (s scales a summed gradient to the mean),
+//             U = M, or the Nesterov input s G + mu M when requested;
+//   update    W <- W - lr (rms O + wd W).
+// ---------------------------------------------------------------------------
+__global__ void momentum_flat_kernel(float* __restrict__ m, const float* __restrict__ g, float* __restrict__ u,
+                                     long long n, float mu, float gs, int nesterov, int vec) {
+    pdl_wait();
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    const long long t0 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long nv = vec ? n / 4 : 0;
+    for (long long i = t0; i < nv; i += stride) {
+        float4 mv = reinterpret_cast<const float4*>(m)[i];
+        float4 gv = reinterpret_cast<const float4*>(g)[i];
+        gv.x = __fmul_rn(gv.x, gs); gv.y = __fmul_rn(gv.y, gs);
+        gv.z = __fmul_rn(gv.z, gs); gv.w = __fmul_rn(gv.w, gs);
+        mv.x = __fmaf_rn(mu, mv.x, gv.x); mv.y = __fmaf_rn(mu, mv.y, gv.y);
+        mv.z = __fmaf_rn(mu, mv.z, gv.z); mv.w = __fmaf_rn(mu, mv.w, gv.w);
+        reinterpret_cast<float4*>(m)[i] = mv;
+        if (u) {
+            float4 uv = mv;
+            if (nesterov)
+                uv = make_float4(__fmaf_rn(mu, mv.x, gv.x), __fmaf_rn(mu, mv.y, gv.y), __fmaf_rn(mu, mv.z, gv.z),
+                                 __fmaf_rn(mu, mv.w, gv.w));
+            reinterpret_cast<float4*>(u)[i] = uv;
+        }
+    }
+    for (long long i = nv * 4 + t0; i < n; i += stride) {
+        const float gv = __fmul_rn(g[i], gs);
+        const float mv = __fmaf_rn(mu, m[i], gv);
+        m[i] = mv;
+        if (u) u[i] = nesterov ? __fmaf_rn(mu, mv, gv) : mv;
+    }
+    pdl_trigger();
+}
+
+__global__ void update_flat_kernel(float* __restrict__ w, const float* __restrict__ o, long long n, float lr,
+                                   float rms, float wd, int vec) {
+    pdl_wait();
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    const long long t0 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long nv = vec ? n / 4 : 0;
+    for (long long i = t0; i < nv; i += stride) {
+        float4 wv = reinterpret_cast<const float4*>(w)[i];
+        const float4 ov = reinterpret_cast<const float4*>(o)[i];
+        wv.x = muon_update_elem(wv.x, ov.x, lr, rms, wd);
+        wv.y = muon_update_elem(wv.y, ov.y, lr, rms, wd);
+        wv.z = muon_update_elem(wv.z, ov.z, lr, rms, wd);
+        wv.w = muon_update_elem(wv.w, ov.w, lr, rms, wd);
+        reinterpret_cast<float4*>(w)[i] = wv;
+    }
+    for (long long i = nv * 4 + t0; i < n; i += stride) w[i] = muon_update_elem(w[i], o[i], lr, rms, wd);
+    pdl_trigger();
+}
+
+static unsigned flat_blocks(long long n) {
+    long long b = (n / 4 + 255) / 256;
+    if (b < 1) b = 1;
+    if (b > (long long)num_sms() * 8) b = (long long)num_sms() * 8;
+    return (unsigned)b;
+}
+
+cudaError_t launch_momentum_flat(float* m, const float* g, float* u, long long n, float mu, float gs,
+                                 int nesterov, cudaStream_t stream) {
+    if (n <= 0) return cudaSuccess;
+    const int vec = ((reinterpret_cast<uintptr_t>(m) | reinterpret_cast<uintptr_t>(g) |
+                      (u ? reinterpret_cast<uintptr_t>(u) : 0)) & 15) == 0;
+    TraceScope ts("muon_momentum_shard", stream);
+    return launch_pdl(momentum_flat_kernel, dim3(flat_blocks(n)), dim3(256), 0, stream, m, g, u, n, mu, gs,
+                      nesterov, vec);
+}
+
+cudaError_t launch_update_flat(float* w, const float* o, long long n, float lr, float rms, float wd,
+                               cudaStream_t stream) {
+    if (n <= 0) return cudaSuccess;
+    const int vec = ((reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(o)) & 15) == 0;
+    TraceScope ts("muon_update_shard", stream);
+    return launch_pdl(update_flat_kernel, dim3(flat_blocks(n)), dim3(256), 0, stream, w, o, n, lr, rms, wd, vec);
+}
+
+// ---------------------------------------------------------------------------
+// Order-preserving int32 keys of fp32 S_max values, so the per-head maximum
+// over data-parallel ranks is one all-reduce(MAX) of integers: a < b implies
+// key(a) < key(b), -0 sits just below +0, and every NaN maps to the largest
+// key, so a NaN max logit on any rank reaches every rank (a float max
+// reduction may drop it).  Decoding inverts the map (NaNs come back as one
+// quiet NaN).
+// ---------------------------------------------------------------------------
+MC_D int smax_key(float f) {
+    if (f != f) return 0x7FFFFFFF;
+    const int b = __float_as_int(f);
+    return b >= 0 ? b : (b ^ 0x7FFFFFFF);
+}
+MC_D float smax_unkey(int k) { return __int_as_float(k >= 0 ? k : (k ^ 0x7FFFFFFF)); }
+
+__global__ void smax_keys_kernel(const float* s, int* keys, const int* kin, float* sout, int n) {
+    pdl_wait();
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        if (s) keys[i] = smax_key(s[i]);
+        else sout[i] = smax_unkey(kin[i]);
+    }
+    pdl_trigger();
+}
+
+cudaError_t launch_smax_keys(const float* s, int* keys, const int* kin, float* sout, int n, cudaStream_t stream) {
+    if (n <= 0) return cudaSuccess;
+    const int blocks = (n + 255) / 256 < 64 ? (n + 255) / 256 : 64;
+    TraceScope ts("smax_keys", stream);
+    return launch_pdl(smax_keys_kernel, dim3(blocks), dim3(256), 0, stream, s, keys, kin, sout, n);
 }
 
 // s = 1 / (||U||_F + eps) from the tile partials, summed in a fixed order

@@ -228,6 +228,12 @@ struct MatBatch {
     int x_f16;           // modes 2/3: X holds fp16 (the Newton-Schulz output)
 };
 cudaError_t launch_mat_pass(const MatBatch& b, cudaStream_t stream);
+// flat passes over one ZeRO-1 shard, and the S_max <-> int32 key maps
+cudaError_t launch_momentum_flat(float* m, const float* g, float* u, long long n, float mu, float gs,
+                                 int nesterov, cudaStream_t stream);
+cudaError_t launch_update_flat(float* w, const float* o, long long n, float lr, float rms, float wd,
+                               cudaStream_t stream);
+cudaError_t launch_smax_keys(const float* s, int* keys, const int* kin, float* sout, int n, cudaStream_t stream);
 // bounded-wait self-test (one CTA of two waiting warps; elementwise.cu)
 cudaError_t launch_wait_selftest(uint64_t limit_ns, long long* out, cudaStream_t stream);
 
