@@ -228,7 +228,7 @@ static bool weight_problem(GemmProblem& q, const void* a, int64_t a_rows, int64_
                            const void* w, int64_t K, int64_t N, void* out, int64_t out_ld, int f16) {
     memset(&q, 0, sizeof(q));
     if (!make_tmap_3d(&q.tmA, a, a_inner, a_rows, 1, a_ld, 0, kBK, kBM, f16)) return false;
-    if (!make_tmap_3d(&q.tmB, w, N, K, 1, N, 0, 64, kStageK, f16)) return false;
+    if (!make_tmap_3d(&q.tmB, w, N, K, 1, N, 0, 64, kStageKPair, f16)) return false;
     q.ab_f16 = f16;
     q.out_kind = kOutF16;
     q.M = (int)a_rows;
@@ -902,7 +902,8 @@ bool ns_problem(GemmProblem& q, const NsPlan& P, const NsGroup& gr, int kind, in
         q.beta = b;
     } else {
         if (!make_tmap_3d(&q.tmA, gr.Bm, mp, mp, cnt, mp, mp * mp, kBK, kBM, in_f16)) return false;
-        if (!make_tmap_3d(&q.tmB, gr.X[xin], np, mp, cnt, np, mp * np, 64, kStageK, in_f16)) return false;
+        if (!make_tmap_3d(&q.tmB, gr.X[xin], np, mp, cnt, np, mp * np, 64, stage_k_for(tile_m), in_f16))
+            return false;
         q.b_mn = 1;
         q.M = (int)mp;
         q.N = (int)np;
@@ -1107,7 +1108,7 @@ mc_status mc_gemm_bf16(const void* a, const void* b, void* c, mc_dtype c_type, i
         const uint32_t brows = P.tile_m == kBM ? kBN : kBN / 2;
         if (!make_tmap_3d(&q.tmB, b, k, n, z, k, n * k, kBK, brows, 0)) return MC_ERR_INVALID_ARG;
     } else {
-        if (!make_tmap_3d(&q.tmB, b, n, k, z, n, k * n, 64, kStageK, 0)) return MC_ERR_INVALID_ARG;
+        if (!make_tmap_3d(&q.tmB, b, n, k, z, n, k * n, 64, kStageKPair, 0)) return MC_ERR_INVALID_ARG;
         q.b_mn = 1;
     }
     q.M = M;

@@ -18,13 +18,11 @@
 
 namespace mc {
 
-// A stage: K = kStageK in chunks of kBK (one 128-byte swizzle row each).
-// Eight MMAs per commit: a commit and the producer's wait on it cost about
-// as much as four N = 128 MMAs, so four MMAs per commit ran at half the
-// tensor rate at N = 128 (measured); eight per commit keep it near full.
-constexpr int kKChunks = kStageK / kBK;
+// A stage: K = KS in chunks of kBK (one 128-byte swizzle row each).
+// Single CTAs (N = 128) take KS = 128, eight MMAs per commit: a commit and
+// the producer's wait on it cost about as much as four N = 128 MMAs, so four
+// MMAs per commit ran at half the tensor rate at N = 128 (measured).
 constexpr int kAChunkBytes = kBM * kBK * 2;            // 16 KB
-constexpr int kAStageBytes = kAChunkBytes * kKChunks;  // 32 KB
 // warp 0 and warp 6: TMA producers (the A and the B half of every stage:
 // one thread issues TMA loads at about half the rate two threads in
 // different warps reach); warp 1: MMA issuer; warps 2..5: epilogue
@@ -54,17 +52,19 @@ MC_D int stage_off(bool swz, int r, int v) { return swz ? r * 64 + ((v ^ (r & 7)
 // parameters.
 constexpr int kTailBytes = 384;
 constexpr int kProbStageBytes = 2 * kPhaseProbs * (int)sizeof(GemmProblem);
-template <int BN, int STAGES, bool PAIR = false>
+template <int BN, int STAGES, bool PAIR, int KS>
 struct TileCfg {
+    static constexpr int kKChunks = KS / kBK;
+    static constexpr int kAStageBytes = kAChunkBytes * kKChunks;
     // a pair computes a 256 x BN tile: each CTA holds 128 rows of A and BN / 2
     // rows (K-major) or columns (MN-major) of B; the MMA reads both halves
     static constexpr int kTileM = PAIR ? 2 * kBM : kBM;
     static constexpr int kBRows = PAIR ? BN / 2 : BN;
     // K-major B: kKChunks chunks of kBRows rows x 128 bytes; MN-major B:
-    // kBRows / 64 column chunks of kStageK rows x 128 bytes
+    // kBRows / 64 column chunks of KS rows x 128 bytes
     static constexpr int kBChunkK = kBRows * kBK * 2;
-    static constexpr int kBChunkMN = kStageK * 128;
-    static constexpr int kBStage = kBRows * kStageK * 2;
+    static constexpr int kBChunkMN = KS * 128;
+    static constexpr int kBStage = kBRows * KS * 2;
     static constexpr int kSmem = STAGES * (kAStageBytes + kBStage) + 4 * kEpiWarpBytes + 1024 + kTailBytes +
                                  64 + kProbStageBytes;
     static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
@@ -469,9 +469,11 @@ MC_D void norm_prephase(const GemmParamsT<MAXP>& P, double* red) {
     }
 }
 
-template <int MAXP, int BN, int STAGES, bool PAIR>
+template <int MAXP, int BN, int STAGES, bool PAIR, int KS>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParamsT<MAXP> P) {
-    using Cfg = TileCfg<BN, STAGES, PAIR>;
+    using Cfg = TileCfg<BN, STAGES, PAIR, KS>;
+    constexpr int kKChunks = Cfg::kKChunks;
+    constexpr int kAStageBytes = Cfg::kAStageBytes;
     constexpr int TM = Cfg::kTileM;
     constexpr int kBStageBytes = Cfg::kBStage;
     constexpr int kGemmStages = STAGES;
@@ -567,7 +569,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                     const CUtensorMap* tmA = &P.p[pb + pi].tmA;
                     const CUtensorMap* tmB = &P.p[pb + pi].tmB;
                     const int b_mn = q.b_mn;
-                    const int nk = (q.K + kStageK - 1) / kStageK;
+                    const int nk = (q.K + KS - 1) / KS;
                     for (int kb = 0; kb < nk; ++kb) {
                         if (!mbar_wait(&tail->empty[stage], phase ^ 1, abort_flag, P.status)) {
                             ok = false;
@@ -575,7 +577,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                         }
                         uint8_t* a = sA + stage * kAStageBytes;
                         uint8_t* b = sB + stage * kBStageBytes;
-                        const int k0 = kb * kStageK;
+                        const int k0 = kb * KS;
                         if constexpr (PAIR) {
                             // both CTAs' halves complete on the leader's full barrier
                             const uint32_t fb = mapa_shared(smem_u32(&tail->full[stage]), 0);
@@ -628,7 +630,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 int pi, z, tm, tn;
                 decode_tile<BN, TM>(sp, np, t, pi, z, tm, tn);
                 const GemmProblem& q = sp[pi];
-                const int nk = (q.K + kStageK - 1) / kStageK;
+                const int nk = (q.K + KS - 1) / KS;
                 const int b_mn = q.b_mn;
                 const uint32_t idesc = idesc_f16kind(TM, BN, b_mn, q.ab_f16);
                 if (!mbar_wait(&tail->tempty[acc], aphase ^ 1, abort_flag, P.status)) {
@@ -652,7 +654,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                         const uint64_t b_d = b_mn ? sw128_desc(smem_u32(sB + stage * kBStageBytes), Cfg::kBChunkMN, 1024)
                                                   : sw128_desc(smem_u32(sB + stage * kBStageBytes), 16, 1024);
 #pragma unroll
-                        for (int k = 0; k < kStageK / 16; ++k) {
+                        for (int k = 0; k < KS / 16; ++k) {
                             const uint64_t ad = a_d + (uint64_t)((k >> 2) * (kAChunkBytes >> 4) + (k & 3) * 2);
                             const uint64_t bd = b_mn ? b_d + (uint64_t)(k * (2048 >> 4))
                                                      : b_d + (uint64_t)((k >> 2) * (Cfg::kBChunkK >> 4) + (k & 3) * 2);
@@ -771,15 +773,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     }
 }
 
-template <int MAXP, int BN, int STAGES, bool PAIR>
+template <int MAXP, int BN, int STAGES, bool PAIR, int KS>
 static cudaError_t set_smem_attr() {
     static bool attr_set[64] = {false};
     int dev = current_device();
     if (dev < 0) return cudaErrorInvalidDevice;
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<MAXP, BN, STAGES, PAIR>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<MAXP, BN, STAGES, PAIR, KS>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             TileCfg<BN, STAGES, PAIR>::kSmem);
+                                             TileCfg<BN, STAGES, PAIR, KS>::kSmem);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
@@ -801,11 +803,12 @@ static bool phases_fit(const GemmParamsT<MAXP>& P) {
 // One persistent CTA (pair: one cluster of two CTAs) per SM (pair of SMs),
 // no more than there are tiles; cooperative launches keep every CTA resident
 // for the grid barriers between phases.
-template <int MAXP, int BN, int STAGES, bool PAIR>
+template <int MAXP, int BN, int STAGES, bool PAIR, int KS>
 static cudaError_t launch_cfg(const GemmParamsT<MAXP>& P, bool coop, cudaStream_t stream, const char* label) {
-    using Cfg = TileCfg<BN, STAGES, PAIR>;
+    using Cfg = TileCfg<BN, STAGES, PAIR, KS>;
+    static_assert(Cfg::kSmem <= 232448, "shared memory");
     if (P.tile_m != Cfg::kTileM || P.bn != BN) return cudaErrorInvalidValue;
-    cudaError_t e = set_smem_attr<MAXP, BN, STAGES, PAIR>();
+    cudaError_t e = set_smem_attr<MAXP, BN, STAGES, PAIR, KS>();
     if (e != cudaSuccess) return e;
     int units = PAIR ? num_sms() / 2 : num_sms();
     if (!coop && units > P.total_tiles) units = P.total_tiles;
@@ -835,24 +838,25 @@ static cudaError_t launch_cfg(const GemmParamsT<MAXP>& P, bool coop, cudaStream_
     cfg.attrs = attr;
     cfg.numAttrs = na;
     TraceScope ts(label, stream);
-    e = cudaLaunchKernelEx(&cfg, gemm_kernel<MAXP, BN, STAGES, PAIR>, P);
+    e = cudaLaunchKernelEx(&cfg, gemm_kernel<MAXP, BN, STAGES, PAIR, KS>, P);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-// Configurations: 256 x 256 tiles on CTA pairs with 3 stages of 64 KB per
-// SM (projections, plain GEMMs, large Newton-Schulz batches); 128 x 128
-// tiles on single CTAs with 3 stages of 64 KB (small Newton-Schulz batches).
+// Configurations: 256 x 256 tiles on CTA pairs (projections, plain GEMMs,
+// large Newton-Schulz batches) and 128 x 128 tiles on single CTAs (small
+// Newton-Schulz batches), with the stage shapes of internal.h.
 cudaError_t launch_gemm(const GemmParams& P, cudaStream_t stream, const char* label) {
     if (P.total_tiles <= 0) return cudaSuccess;
     if (!phases_fit(P)) return cudaErrorInvalidValue;
-    return launch_cfg<kMaxProblems, kBN, 3, true>(P, false, stream, label);
+    return launch_cfg<kMaxProblems, kBN, kStagesPair, true, kStageKPair>(P, false, stream, label);
 }
 
 cudaError_t launch_gemm_multi(const GemmParamsMulti& P, cudaStream_t stream, const char* label) {
     if (P.total_tiles <= 0) return cudaSuccess;
     if (!phases_fit(P)) return cudaErrorInvalidValue;
-    if (P.tile_m == 2 * kBM) return launch_cfg<kMaxProblemsMulti, kBN, 3, true>(P, true, stream, label);
-    return launch_cfg<kMaxProblemsMulti, 128, 3, false>(P, true, stream, label);
+    if (P.tile_m == 2 * kBM)
+        return launch_cfg<kMaxProblemsMulti, kBN, kStagesPair, true, kStageKPair>(P, true, stream, label);
+    return launch_cfg<kMaxProblemsMulti, 128, kStagesSingle, false, kStageKSingle>(P, true, stream, label);
 }
 
 }  // namespace mc

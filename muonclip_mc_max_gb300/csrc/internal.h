@@ -19,7 +19,20 @@ namespace mc {
 constexpr int kBM = 128;  // UMMA M (TMEM lanes)
 constexpr int kBN = 256;  // UMMA N (TMEM columns per accumulator)
 constexpr int kBK = 64;   // K of one 128-byte swizzle row of bf16: one TMA box, one descriptor chunk
-constexpr int kStageK = 128;  // K per pipeline stage: two such chunks, 8 MMAs (K = 16) per commit
+// K per pipeline stage and ring depth of the two GEMM configurations: CTA
+// pairs (256-wide tiles) and single CTAs (128 x 128 tiles).  A stage holds
+// K / 64 swizzle chunks; its MMAs (K = 16 each) share one commit.
+#ifndef MC_PAIR_STAGE_K
+#define MC_PAIR_STAGE_K 128
+#endif
+#ifndef MC_PAIR_STAGES
+#define MC_PAIR_STAGES 3
+#endif
+constexpr int kStageKPair = MC_PAIR_STAGE_K;
+constexpr int kStagesPair = MC_PAIR_STAGES;
+constexpr int kStageKSingle = 128;
+constexpr int kStagesSingle = 3;
+constexpr int stage_k_for(int tile_m) { return tile_m == 2 * kBM ? kStageKPair : kStageKSingle; }
 constexpr int kMaxProblems = 4;        // problems of a single-phase launch
 constexpr int kMaxProblemsMulti = 48;  // problems of a multi-phase launch (kernel parameters < 32 KB)
 constexpr int kMaxPhases = 16;
