@@ -29,7 +29,7 @@ __all__ = [
     "NS_COEFFS", "load", "bf16_to_f64", "f64_to_bf16_bits", "max_logits_mha",
     "max_logits_mla", "gamma", "qk_clip_mha", "qk_clip_mla", "qk_clip_global",
     "newton_schulz", "muon_step", "max_logits_mha_np", "max_logits_mla_np", "newton_schulz_np",
-    "muon_step_np",
+    "muon_step_np", "attention_mha", "attention_mha_np", "attention_mla", "attention_mla_np",
 ]
 
 # Quintic coefficients (a, b, c) of "Notes on Muon blog", section "Algorithm";
@@ -65,6 +65,8 @@ def load():
     lib.oracle_max_logits_mla.restype = I
     lib.oracle_attention_mha.argtypes = [_dp, _dp, _dp, I, I, I, I, I, _dp, _dp]
     lib.oracle_attention_mha.restype = I
+    lib.oracle_attention_mla.argtypes = [_dp, _dp, _dp, _dp, I, I, I, I, I, I, I, _dp, _dp]
+    lib.oracle_attention_mla.restype = I
     lib.oracle_gamma.argtypes = [_fp, I, F, _fp, _fp]
     lib.oracle_gamma.restype = None
     lib.oracle_qk_clip_mha.argtypes = [V, V, I, I, I, I, _fp, F, _fp]
@@ -195,6 +197,27 @@ def attention_mha(q, k, v, H: int, dh: int, causal: bool = False):
                                   _ptr(s))
     if rc:
         raise RuntimeError(f"oracle_attention_mha failed ({rc})")
+    return o, s
+
+
+def attention_mla(q, k_c, k_r, v, H: int, nope: int, rope: int, dv: int, causal: bool = True):
+    """MLA softmax attention forward in fp64 with the max logit taken along.
+
+    q [B, T, H*(nope+rope)] (per head q^C then q^R, RoPE applied), k_c
+    [B, T, H*nope], k_r [B, T, rope] (shared by every head), v [B, T, H*dv].
+    Returns (o [B, T, H*dv], s_bh [B, H]) with s_bh = max_{i,j} (q^C_i.k^C_j
+    + q^R_i.k^R_j) / sqrt(nope + rope) over allowed pairs."""
+    lib = load()
+    Q, KC, KR, V = _to_f64(q), _to_f64(k_c), _to_f64(k_r), _to_f64(v)
+    B, T, W = Q.shape
+    assert W == H * (nope + rope) and KC.shape == (B, T, H * nope) and KR.shape == (B, T, rope)
+    assert V.shape == (B, T, H * dv)
+    o = np.empty((B, T, H * dv))
+    s = np.empty((B, H))
+    rc = lib.oracle_attention_mla(_ptr(Q), _ptr(KC), _ptr(KR), _ptr(V), B, T, H, nope, rope, dv,
+                                  int(causal), _ptr(o), _ptr(s))
+    if rc:
+        raise RuntimeError(f"oracle_attention_mla failed ({rc})")
     return o, s
 
 
@@ -394,6 +417,29 @@ def attention_mha_np(q, k, v, H: int, dh: int, causal: bool = False, batches=Non
             s_bh[ib, ih] = s.max()
             p = np.exp(s - s.max(axis=1, keepdims=True))
             o[ib, :, ih] = (p @ V[b][:, cols]) / p.sum(axis=1, keepdims=True)
+    return o, s_bh
+
+
+def attention_mla_np(q, k_c, k_r, v, H: int, nope: int, rope: int, dv: int, causal: bool = True,
+                     batches=None, heads=None):
+    """As attention_mla, with library GEMMs (fp64), for the listed
+    (batch, head) pairs: returns (o [nb, T, nh, dv], s_bh [nb, nh])."""
+    Q, KC, KR, V = _to_f64(q), _to_f64(k_c), _to_f64(k_r), _to_f64(v)
+    B, T, _ = Q.shape
+    batches = list(range(B)) if batches is None else list(batches)
+    heads = list(range(H)) if heads is None else list(heads)
+    dq = nope + rope
+    o = np.empty((len(batches), T, len(heads), dv))
+    s_bh = np.empty((len(batches), len(heads)))
+    mask = np.tril(np.ones((T, T), dtype=bool)) if causal else np.ones((T, T), dtype=bool)
+    for ib, b in enumerate(batches):
+        for ih, h in enumerate(heads):
+            qh = Q[b][:, h * dq:(h + 1) * dq]
+            s = (qh[:, :nope] @ KC[b][:, h * nope:(h + 1) * nope].T + qh[:, nope:] @ KR[b].T) / np.sqrt(dq)
+            s = np.where(mask, s, -np.inf)
+            s_bh[ib, ih] = s.max()
+            p = np.exp(s - s.max(axis=1, keepdims=True))
+            o[ib, :, ih] = (p @ V[b][:, h * dv:(h + 1) * dv]) / p.sum(axis=1, keepdims=True)
     return o, s_bh
 
 

@@ -41,7 +41,9 @@
  *   - Attention forward (the row that takes the max logit inside the forward
  *     pass): O_i = sum_j softmax_j(s_ij / sqrt(dh)) v_j with s_ij = q_i . k_j
  *     over the keys j the mask allows ([K2-zh 2.1] calls S the largest
- *     softmax input: the logits are the inputs of this softmax).
+ *     softmax input: the logits are the inputs of this softmax).  MLA:
+ *     s_ij = q^C_i . k^C_j + q^R_i . k^R_j with the shared k^R, d = nope +
+ *     rope, and a value head dimension of its own.
  *
  * Parity status: every function here is pinned by the CPU tests against
  * closed forms, special cases, library routines or brute force (see
@@ -294,6 +296,67 @@ int oracle_attention_mha(const double* q, const double* k, const double* v, int 
                         for (int f = 0; f < dh; ++f) oi[f] += p * vj[f];
                     }
                     for (int f = 0; f < dh; ++f) oi[f] /= l;
+                }
+                free(s);
+            }
+            s_bh[(long)b * H + h] = saw_nan ? NAN : best;
+        }
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * MLA attention forward with the max logit taken along.  Per head h the
+ * logit is the content dot product plus the rope dot product against the
+ * key rope part that every head shares ([K2-review] MLA table: q^C, k^C per
+ * head, q^R per head, k^R shared), over the q.k dimension d = nope + rope:
+ *   s_ij = (q^C_i . k^C_j + q^R_i . k^R_j) / sqrt(nope + rope)
+ *   O_i  = sum_j softmax_j(s_ij) v_j          (j <= i when causal)
+ * q [B][T][H][nope + rope] (q^C then q^R of each head, RoPE applied),
+ * kc [B][T][H][nope], kr [B][T][rope], v [B][T][H][dv] -> o [B][T][H][dv];
+ * s_bh[b][h] = max_{i,j} s_ij (NaN if any logit of (b, h) is NaN).
+ */
+int oracle_attention_mla(const double* q, const double* kc, const double* kr, const double* v, int B, int T,
+                         int H, int nope, int rope, int dv, int causal, double* o, double* s_bh) {
+    if (B <= 0 || T <= 0 || H <= 0 || nope < 0 || rope < 0 || nope + rope <= 0 || dv <= 0) return ORACLE_ERR_ARG;
+    const int dq = nope + rope;
+    const double scale = 1.0 / sqrt((double)dq);
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < H; ++h) {
+            double best = -INFINITY;
+            int saw_nan = 0;
+#pragma omp parallel for schedule(dynamic, 4) reduction(max : best) reduction(| : saw_nan)
+            for (long i = 0; i < T; ++i) {
+                const double* qi = q + (((long)b * T + i) * H + h) * dq;
+                const long jend = causal ? i + 1 : T;
+                double* s = (double*)malloc(sizeof(double) * (size_t)jend);
+                double m = -INFINITY;
+                int row_nan = 0;
+                for (long j = 0; j < jend; ++j) {
+                    const double* kcj = kc + (((long)b * T + j) * H + h) * nope;
+                    const double* krj = kr + ((long)b * T + j) * rope;
+                    double d = 0.0;
+                    for (int f = 0; f < nope; ++f) d += qi[f] * kcj[f];
+                    for (int f = 0; f < rope; ++f) d += qi[nope + f] * krj[f];
+                    s[j] = d * scale;
+                    if (isnan(d)) row_nan = 1;
+                    else if (s[j] > m) m = s[j];
+                }
+                double* oi = o + (((long)b * T + i) * H + h) * dv;
+                if (row_nan) {
+                    saw_nan = 1;
+                    for (int f = 0; f < dv; ++f) oi[f] = NAN;
+                } else {
+                    if (m > best) best = m;
+                    double l = 0.0;
+                    for (int f = 0; f < dv; ++f) oi[f] = 0.0;
+                    for (long j = 0; j < jend; ++j) {
+                        const double p = exp(s[j] - m);
+                        const double* vj = v + (((long)b * T + j) * H + h) * dv;
+                        l += p;
+                        for (int f = 0; f < dv; ++f) oi[f] += p * vj[f];
+                    }
+                    for (int f = 0; f < dv; ++f) oi[f] /= l;
                 }
                 free(s);
             }

@@ -585,3 +585,93 @@ def test_attention_nan_logit_propagates():
     q[0, 2, 1] = np.nan
     o, s = oracle.attention_mha(q, k, v, 1, 4, True)
     assert np.isnan(s).all() and np.isnan(o[0, 2]).all() and np.isfinite(o[0, 1]).all()
+
+
+# ---------------------------------------------------------------------------
+# MLA attention forward with the max logit taken along
+# ---------------------------------------------------------------------------
+
+def _mla_qkv(B, T, H, nope, rope, dv, seed, scale=1.0):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((B, T, H * (nope + rope))) * scale
+    kc = rng.standard_normal((B, T, H * nope))
+    kr = rng.standard_normal((B, T, rope))
+    v = rng.standard_normal((B, T, H * dv))
+    return q, kc, kr, v
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_mla_reduces_to_mha_with_shared_rope_keys(causal):
+    """MLA attention is MHA attention over d = nope + rope once every head's
+    key is [k^C_h | k^R] (the shared k^R repeated per head) and the values
+    are padded with zeros to d: the MHA output's first dv columns of each
+    head, and its max logit, are the MLA ones."""
+    B, T, H, nope, rope, dv = 2, 9, 3, 6, 4, 7
+    q, kc, kr, v = _mla_qkv(B, T, H, nope, rope, dv, 1201)
+    dq = nope + rope
+    k_full = np.concatenate([np.concatenate([kc[..., h * nope:(h + 1) * nope], kr], axis=-1)
+                             for h in range(H)], axis=-1)
+    v_pad = np.concatenate([np.concatenate([v[..., h * dv:(h + 1) * dv],
+                                            np.zeros((B, T, dq - dv))], axis=-1) for h in range(H)],
+                           axis=-1)
+    o, s = oracle.attention_mla(q, kc, kr, v, H, nope, rope, dv, causal)
+    o2, s2 = oracle.attention_mha(q, k_full, v_pad, H, dq, causal)
+    o2 = o2.reshape(B, T, H, dq)
+    assert np.allclose(o.reshape(B, T, H, dv), o2[..., :dv], rtol=1e-13, atol=1e-14)
+    assert np.all(o2[..., dv:] == 0.0)
+    assert np.allclose(s, s2, rtol=1e-14, atol=0)
+
+
+def test_attention_mla_c_matches_library_gemm_formulation():
+    q, kc, kr, v = _mla_qkv(2, 11, 2, 8, 4, 5, 1202)
+    for causal in (False, True):
+        o, s = oracle.attention_mla(q, kc, kr, v, 2, 8, 4, 5, causal)
+        o2, s2 = oracle.attention_mla_np(q, kc, kr, v, 2, 8, 4, 5, causal)
+        assert np.abs(o.reshape(2, 11, 2, 5) - o2).max() < 1e-12
+        assert np.abs(s - s2).max() < 1e-12
+
+
+def test_attention_mla_without_query_rope_ignores_the_shared_key_rope():
+    """q^R = 0: the rope term vanishes, so replacing k^R changes nothing."""
+    q, kc, kr, v = _mla_qkv(1, 8, 2, 6, 4, 3, 1203)
+    q = q.reshape(1, 8, 2, 10)
+    q[..., 6:] = 0.0
+    q = q.reshape(1, 8, 20)
+    o, s = oracle.attention_mla(q, kc, kr, v, 2, 6, 4, 3, True)
+    o2, s2 = oracle.attention_mla(q, kc, 5.0 * kr + 3.0, v, 2, 6, 4, 3, True)
+    assert np.array_equal(o, o2) and np.array_equal(s, s2)
+
+
+def test_attention_mla_single_key_returns_its_value():
+    q, kc, kr, v = _mla_qkv(2, 1, 3, 4, 2, 5, 1204)
+    o, s = oracle.attention_mla(q, kc, kr, v, 3, 4, 2, 5, True)
+    assert np.array_equal(o, v)
+    qh, kch = q.reshape(2, 3, 6), kc.reshape(2, 3, 4)
+    ref = ((qh[..., :4] * kch).sum(-1) + (qh[..., 4:] * kr.reshape(2, 1, 2)).sum(-1)) / np.sqrt(6)
+    assert np.allclose(s, ref, atol=1e-14)
+
+
+def test_attention_mla_max_logit_equals_the_scan_oracle():
+    """S from the MLA attention oracle on the layer's projections (q^C, q^R,
+    k^C, k^R with RoPE) is the max logit of oracle_max_logits_mla on (x, W)."""
+    inp = mc_inputs.mla_layer(B=2, T=24, D=32, H=2, q_lora=16, kv_lora=12, nope=8, rope=4, n_hot=1,
+                              w_std=0.3, seed=1205)
+    x = inp["x"].double().numpy()
+    qa, qb, kva, kb = (inp[n].double().numpy() for n in ("w_qa", "w_qb", "w_kva", "w_kb"))
+    H, nope, rope, base = 2, 8, 4, inp["rope_base"]
+    q = np.empty((2, 24, H * 12))
+    kc = np.empty((2, 24, H * nope))
+    kr = np.empty((2, 24, rope))
+    for b in range(2):
+        cq, ckv = x[b] @ qa, x[b] @ kva
+        kr[b] = oracle._rope_np(ckv[:, 12:], 0, base)
+        for h in range(H):
+            qh = cq @ qb[:, h * 12:(h + 1) * 12]
+            q[b, :, h * 12:h * 12 + nope] = qh[:, :nope]
+            q[b, :, h * 12 + nope:(h + 1) * 12] = oracle._rope_np(qh[:, nope:], 0, base)
+            kc[b, :, h * nope:(h + 1) * nope] = ckv[:, :12] @ kb[:, h * nope:(h + 1) * nope]
+    for causal in (True, False):
+        _, s = oracle.attention_mla(q, kc, kr, np.zeros((2, 24, H)), H, nope, rope, 1, causal)
+        ref = oracle.max_logits_mla(inp["x"], inp["w_qa"], inp["w_qb"], inp["w_kva"], inp["w_kb"], H,
+                                    nope, rope, base, causal)
+        assert np.allclose(s, ref, rtol=1e-12, atol=0)
