@@ -17,7 +17,7 @@ workloads in one process:
     roofline and kernel breakdown).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload c4|c2|c3|c5|attn|attnl] [--no-long-mla]
+                  [--workload c4|c2|c3|c5|attn|attnl|attn_mla] [--no-long-mla]
 
 value     = algorithmic TFLOP/s of the step (scan + Newton-Schulz flops per
             step / device time per step, inputs resident, L2 flushed between
@@ -34,7 +34,8 @@ cpu_baseline = the fp64 oracle on this host's cores on a bounded sample.
 c2 is the MHA layer (x [8,1024,1024], 16 heads of 64, Muon on W_q and W_k).
 attn / attnl time the attention forward that takes the max logit along
 (value = its algorithmic TFLOP/s: 4 flops per allowed (i, j) pair and head
-dimension); they are extra lines, not the default workload.
+dimension), attn_mla the MLA forward (2 (192 + 128) flops per allowed pair
+and head); they are extra lines, not the default workload.
 """
 from __future__ import annotations
 
@@ -394,9 +395,58 @@ class AttnLayer(Workload):
                 f"one head of one sequence over the first {T} tokens, fp64")
 
 
+class AttnMlaLayer(Workload):
+    """attn_mla: the MLA attention forward (K2 shapes: 64 heads, q^C/k^C 128,
+    q^R/k^R 64 with k^R shared, dv 128) with the max logit taken along."""
+
+    def __init__(self, B=2, T=8192, H=64):
+        self.name = "attn_mla"
+        self.B, self.T, self.H, self.causal = B, T, H, True
+        self.desc = (f"MLA attention forward bf16 q [{B},{T},{H}x192], k^C [{B},{T},{H}x128], shared "
+                     f"k^R [{B},{T},64], v [{B},{T},{H}x128] causal, O bf16 and the per-head max logit")
+        pairs = scan_pairs(B, T, True)
+        # 2 flops per multiply-add: q.k over 192 and p.v over 128 per allowed pair and head
+        self.units = {"attn_mla": ("tensor", 2 * pairs * H * (192 + 128))}
+        self.metric = "MLA attention forward with the max logit taken along, TFLOP/s (% bf16 peak)"
+        self.scan_flops = self.units["attn_mla"][1]
+        self.ns_flops = 0
+
+    def make(self, device):
+        import torch
+        s = mc_inputs.attention_mla_qkv(self.B, self.T, self.H, seed=1700, device=device)
+        s["o"] = torch.empty((self.B, self.T, self.H * 128), dtype=torch.bfloat16, device=device)
+        s["s_max"] = torch.empty(self.H, dtype=torch.float32, device=device)
+        return s
+
+    def inputs(self, s):
+        return [s["q"], s["k_c"], s["k_r"], s["v"]]
+
+    def outputs(self, s):
+        return [s["s_max"]]
+
+    def step(self, s, api):
+        self.step_part(s, api, "scan")
+
+    def step_part(self, s, api, part):
+        if part == "scan":
+            api.mc_attention_mla(s["q"], s["k_c"], s["k_r"], s["v"], self.H, causal=True, out=s["o"],
+                                 s_max=s["s_max"])
+
+    def oracle_sample(self, s):
+        import oracle
+        T = min(self.T, 512)
+        q = s["q"][:1, :T, :192].cpu()
+        kc, kr, v = s["k_c"][:1, :T, :128].cpu(), s["k_r"][:1, :T].cpu(), s["v"][:1, :T, :128].cpu()
+        t0 = time.perf_counter()
+        oracle.attention_mla(q, kc, kr, v, 1, 128, 64, 128, True)
+        dt = time.perf_counter() - t0
+        return (2 * scan_pairs(1, T, True) * (192 + 128), dt,
+                f"one head of one sequence over the first {T} tokens, fp64")
+
+
 WORKLOADS = {"c2": lambda: MhaLayer(), "c4": lambda: ExpertBatch(), "c3": lambda: MlaLayer("c3"),
              "c5": lambda: MlaLayer("c5"), "attn": lambda: AttnLayer("attn"),
-             "attnl": lambda: AttnLayer("attnl")}
+             "attnl": lambda: AttnLayer("attnl"), "attn_mla": lambda: AttnMlaLayer()}
 
 
 # ---------------------------------------------------------------------------

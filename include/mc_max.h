@@ -199,6 +199,30 @@ mc_status mc_attention_mha(const void* q, const void* k, const void* v, int B, i
                            int causal, int accumulate, void* o, float* s_max, float* s_max_bh,
                            void* ws, size_t ws_bytes, mc_stream_t stream);
 
+/*
+ * The same for an MLA layer (Kimi K2's attention; the K2 review's MLA
+ * table: per-head content parts q^C, k^C, per-head q^R and a rope key k^R
+ * that every head shares), with the max logit of the MuonClip step taken
+ * along:
+ *   s_ij = (q^C_i . k^C_j + q^R_i . k^R_j) / sqrt(nope + rope)
+ *   O_i  = sum_j softmax_j(s_ij) v_j        (j <= i when causal)
+ *   s_max[h] = max over sequences and (i, j) of s_ij.
+ *   q    device bf16 [B][T][H*(nope+rope)]: per head q^C then q^R (RoPE applied)
+ *   k_c  device bf16 [B][T][H*nope]
+ *   k_r  device bf16 rows of kr_ld elements, [B][T][kr_ld]; k^R is columns
+ *        [kr_col, kr_col + rope) (e.g. the rope part of [c_KV | k^R])
+ *   v    device bf16 [B][T][H*dv];  o  device bf16 [B][T][H*dv], written
+ * Supported: nope = 128, rope = 64, dv = 128 (K2's MLA; else
+ * MC_ERR_UNSUPPORTED).  kr_ld and kr_col multiples of 8; pointers 16-byte
+ * aligned; o must not alias an input.  Precision, NaN handling, s_max_bh,
+ * accumulate and the workspace (mc_attention_mha_workspace_size(B, H)) as
+ * for mc_attention_mha.
+ */
+mc_status mc_attention_mla(const void* q, const void* k_c, const void* k_r, int kr_ld, int kr_col,
+                           const void* v, int B, int T, int H, int nope, int rope, int dv,
+                           int causal, int accumulate, void* o, float* s_max, float* s_max_bh,
+                           void* ws, size_t ws_bytes, mc_stream_t stream);
+
 /* ======================================================================
  * (2) QK-Clip
  * ====================================================================== */

@@ -197,3 +197,15 @@ def attention_qkv(B, T, H, dh, seed, device="cpu", q_std=1.0):
     k = _randn((B, T, H * dh), g, device).to(torch.bfloat16)
     v = _randn((B, T, H * dh), g, device).to(torch.bfloat16)
     return {"q": q, "k": k, "v": v, "H": H, "dh": dh}
+
+
+def attention_mla_qkv(B, T, H, seed, device="cpu", q_std=1.0, nope=128, rope=64, dv=128):
+    """bf16 inputs of the MLA attention forward, N(0, 1) (q scaled by q_std):
+    q [B, T, H*(nope+rope)] (per head q^C then q^R), k_c [B, T, H*nope], the
+    shared k_r [B, T, rope] and v [B, T, H*dv]."""
+    g = _gen(seed, device)
+    q = _randn((B, T, H * (nope + rope)), g, device, std=q_std).to(torch.bfloat16)
+    k_c = _randn((B, T, H * nope), g, device).to(torch.bfloat16)
+    k_r = _randn((B, T, rope), g, device).to(torch.bfloat16)
+    v = _randn((B, T, H * dv), g, device).to(torch.bfloat16)
+    return {"q": q, "k_c": k_c, "k_r": k_r, "v": v, "H": H}

@@ -20,6 +20,7 @@ __all__ = [
     "MCError", "load_library", "header_symbols", "Workspace",
     "mc_status_string", "mc_read_device_status",
     "mc_max_logits_mha", "mc_max_logits_mha_workspace_size", "mc_max_logits_mha_noalloc",
+    "mc_attention_mha", "mc_attention_mha_workspace_size", "mc_attention_mla",
     "MC_NOALLOC_SCRATCH_BYTES",
     "mc_max_logits_mla", "mc_max_logits_mla_workspace_size",
     "mc_qk_clip_mha", "mc_qk_clip_mla", "mc_qk_clip_global",
@@ -91,6 +92,7 @@ def load_library():
         "mc_max_logits_mla": ([ctypes.POINTER(MlaLayer), V, I, I, I, I, V, V, V, S, V], I),
         "mc_attention_mha_workspace_size": ([I, I], S),
         "mc_attention_mha": ([V, V, V, I, I, I, I, I, I, V, V, V, V, S, V], I),
+        "mc_attention_mla": ([V, V, V, I, I, V, I, I, I, I, I, I, I, I, V, V, V, V, S, V], I),
         "mc_qk_clip_mha": ([V, V, I, I, I, I, V, F, V, V], I),
         "mc_qk_clip_mla": ([ctypes.POINTER(MlaLayer), V, F, V, V], I),
         "mc_qk_clip_global": ([V, V, I, I, I, V, I, F, F, V, V], I),
@@ -238,6 +240,35 @@ def mc_attention_mha(q, k, v, H: int, dh: int, causal: bool = False, accumulate:
     _check("mc_attention_mha", lib.mc_attention_mha(
         _ptr(q), _ptr(k), _ptr(v), B, T, H, dh, int(causal), int(accumulate), _ptr(out), _ptr(s_max),
         _ptr(s_max_bh), ws, nb, _stream(stream)))
+    return out, s_max
+
+
+def mc_attention_mla(q, k_c, k_r, v, H: int, nope: int = 128, rope: int = 64, dv: int = 128,
+                     causal: bool = True, accumulate: bool = False, kr_col: int = 0, out=None,
+                     s_max=None, s_max_bh=None, workspace=None, stream=None):
+    """q [B,T,H*(nope+rope)], k_c [B,T,H*nope], k_r [B,T,>= kr_col+rope]
+    (the shared k^R at columns kr_col..), v [B,T,H*dv], all bf16.  Returns
+    (o [B,T,H*dv] bf16, s_max [H] f32): MLA attention with the per-head max
+    logit taken along."""
+    lib = load_library()
+    _need_cuda(q, k_c, k_r, v, out, s_max, s_max_bh)
+    B, T, W = q.shape
+    if W != H * (nope + rope) or k_c.shape != (B, T, H * nope) or v.shape != (B, T, H * dv):
+        raise ValueError("q, k_c, v must be [B, T, H*(nope+rope)], [B, T, H*nope], [B, T, H*dv]")
+    if k_r.dim() != 3 or k_r.shape[:2] != (B, T):
+        raise ValueError("k_r must be [B, T, kr_ld]")
+    for t in (q, k_c, k_r, v):
+        if t.dtype != torch.bfloat16:
+            raise ValueError("q, k_c, k_r, v must be bf16")
+    if out is None:
+        out = torch.empty((B, T, H * dv), dtype=torch.bfloat16, device=q.device)
+    if s_max is None:
+        s_max = torch.empty(H, dtype=torch.float32, device=q.device)
+    ws, nb = _ws(workspace, lib.mc_attention_mha_workspace_size(B, H), q.device)
+    _check("mc_attention_mla", lib.mc_attention_mla(
+        _ptr(q), _ptr(k_c), _ptr(k_r), k_r.shape[2], kr_col, _ptr(v), B, T, H, nope, rope, dv,
+        int(causal), int(accumulate), _ptr(out), _ptr(s_max), _ptr(s_max_bh), ws, nb,
+        _stream(stream)))
     return out, s_max
 
 

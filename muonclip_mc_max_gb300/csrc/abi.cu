@@ -395,6 +395,44 @@ mc_status mc_attention_mha(const void* q, const void* k, const void* v, int B, i
     return MC_OK;
 }
 
+mc_status mc_attention_mla(const void* q, const void* k_c, const void* k_r, int kr_ld, int kr_col, const void* v,
+                           int B, int T, int H, int nope, int rope, int dv, int causal, int accumulate, void* o,
+                           float* s_max, float* s_max_bh, void* ws, size_t ws_bytes, mc_stream_t stream_) {
+    cudaStream_t stream = (cudaStream_t)stream_;
+    if (!q || !k_c || !k_r || !v || !o || !s_max) return MC_ERR_INVALID_ARG;
+    if (B <= 0 || T <= 0 || H <= 0 || nope <= 0 || rope <= 0 || dv <= 0) return MC_ERR_INVALID_ARG;
+    if (nope != 128 || rope != 64 || dv != 128) return MC_ERR_UNSUPPORTED;
+    if ((int64_t)B * T > INT32_MAX || (int64_t)H * 192 > INT32_MAX) return MC_ERR_UNSUPPORTED;
+    if (kr_col < 0 || kr_ld < kr_col + rope || kr_ld % 8 || kr_col % 8) return MC_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_c) || !aligned16(k_r) || !aligned16(v) || !aligned16(o)) return MC_ERR_INVALID_ARG;
+    if (o == q || o == k_c || o == k_r || o == v) return MC_ERR_INVALID_ARG;
+    const size_t need = mc_attention_mha_workspace_size(B, H);
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < need) return MC_ERR_WORKSPACE;
+    unsigned* keys = (unsigned*)ws;
+    MC_CUDA(cudaMemsetAsync(keys, 0, sizeof(unsigned) * ((size_t)B * H + 1), stream));
+    AttnArgs a;
+    memset(&a, 0, sizeof(a));
+    a.q = q;
+    a.k = k_c;
+    a.v = v;
+    a.kr = k_r;
+    a.kr_ld = kr_ld;
+    a.kr_col = kr_col;
+    a.mla = 1;
+    a.o = o;
+    a.B = B;
+    a.T = T;
+    a.H = H;
+    a.dh = nope + rope;
+    a.causal = causal ? 1 : 0;
+    a.keys = keys;
+    a.accumulate = accumulate ? 1 : 0;
+    a.s_max = s_max;
+    a.s_bh = s_max_bh;
+    MC_CUDA(launch_attn(a, stream));
+    return MC_OK;
+}
+
 size_t mc_max_logits_mha_workspace_size(int B, int T, int D, int H, int dh, mc_dtype dtype) {
     if (B <= 0 || T <= 0 || D <= 0 || H <= 0 || dh <= 0) return 0;
     Carve c{nullptr, 0};

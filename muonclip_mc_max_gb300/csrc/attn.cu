@@ -53,6 +53,8 @@ constexpr int kAttnSmem = 1024 + 1024 + kAttnRing;
 
 struct AttnParams {
     CUtensorMap tmQ, tmK, tmV;  // {H*dh, T, B} bf16, box {64, 128}
+    CUtensorMap tmKR;           // MLA: the shared k^R {kr_ld, T, B}, box {64, 128}
+    int kr_col;
     int B, T, H, dh, causal;
     int n_it, n_pair, total_items, band, kst, vst;
     __nv_bfloat16* o;
@@ -538,7 +540,428 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     }
 }
 
+// ---------------------------------------------------------------------------
+// MLA attention forward with the max logit taken along (K2's attention: the
+// K2 review's MLA table).  Per head the logit is q^C.k^C over nope = 128
+// plus q^R.k^R over rope = 64 with the k^R every head shares, d = 192; the
+// values and the output have dv = 128.
+//
+// Same roles and item order as attn_kernel.  S_t = Q_t K_j^T runs over three
+// 64-wide blocks: the two q^C blocks of the head against its k^C blocks and
+// the q^R block against the shared k^R (loaded from its own tensor).  Q, K
+// and V of two tiles fill shared memory (96 + 2 x 48 + 32 KB), so P_t goes
+// to TMEM, over the first 64 columns of S_t (S0 | S1 | O0 | O1 fill the 512
+// columns).  The MMA thread therefore issues S_t(j+1) only after
+// O_t += P_t(j) V_j: the tensor pipe executes one thread's MMAs in issue
+// order, so the product has read P before the next S overwrites it, and the
+// softmax writes P_t(j) only after it has loaded S_t(j) and after the
+// previous product (oready) has read P_t(j-1).
+// ---------------------------------------------------------------------------
+constexpr int kMlaQkBlocks = 3;  // q^C (2 blocks) and q^R (1 block) per head
+
+// S_t = Q_t K^T over the three 64-wide blocks, the blocks in a rolled loop:
+// the MMA warp runs on the smallest register share of the kernel
+MC_D void issue_s_mla(uint32_t d_tmem, uint64_t qd, uint64_t kd, uint32_t idesc) {
+#pragma unroll 1
+    for (int c = 0; c < kMlaQkBlocks; ++c) {
+        const uint64_t boff = (uint64_t)((c * kAttnTile) >> 4);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            umma_bf16(d_tmem, qd + boff + (uint64_t)(k * 2), kd + boff + (uint64_t)(k * 2), idesc, (c | k) != 0);
+    }
+}
+constexpr int kMlaVBlocks = 2;   // dv = 128
+constexpr int kMlaKStages = 2;
+constexpr int kMlaVStages = 1;
+static_assert((2 * kMlaQkBlocks + kMlaKStages * kMlaQkBlocks + kMlaVStages * kMlaVBlocks) * kAttnTile <= kAttnRing,
+              "MLA shared memory");
+
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_mla_kernel(const __grid_constant__ AttnParams P) {
+    constexpr int DV = 128;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    AttnSmemTail* tail = reinterpret_cast<AttnSmemTail*>(smem);
+    uint8_t* sQ = smem + 1024;                                  // tile t: blocks 3t ..
+    uint8_t* sK = sQ + 2 * kMlaQkBlocks * kAttnTile;           // stage s: 3 blocks (k^C, k^C, k^R)
+    uint8_t* sV = sK + kMlaKStages * kMlaQkBlocks * kAttnTile;  // stage s: 2 blocks
+    volatile int* abort_flag = &tail->abort_flag;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kAttnMaxStages; ++s) {
+            mbar_init(&tail->kfull[s], 1);
+            mbar_init(&tail->kempty[s], 1);
+            mbar_init(&tail->vfull[s], 1);
+            mbar_init(&tail->vempty[s], 1);
+        }
+        mbar_init(&tail->qfull, 1);
+        mbar_init(&tail->qempty, 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&tail->sfull[t], 1);
+            mbar_init(&tail->sempty[t], 4);
+            mbar_init(&tail->pfull[t], 4);
+            mbar_init(&tail->oready[t], 1);
+            mbar_init(&tail->oempty[t], 4);
+        }
+        mbar_init(&tail->drain, 1);
+        tail->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&P.tmQ);
+        tma_prefetch_desc(&P.tmK);
+        tma_prefetch_desc(&P.tmKR);
+        tma_prefetch_desc(&P.tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(&tail->tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = tail->tmem_base;  // S_t (and P_t) at 128 t, O_t at 256 + 128 t
+    pdl_wait();
+
+    if (warp < 4) {
+    setmaxnreg_dec<attn_regs_low<64>()>();  // the dh = 64 split: P goes to TMEM here too
+    if (warp == 0 || warp == 2) {
+        // ---------------- TMA producers: Q and K (warp 0), V (warp 2) ----------------
+        if (lane == 0) {
+            const bool is_k = warp == 0;
+            const int nst = is_k ? kMlaKStages : kMlaVStages;
+            const int nblk = is_k ? kMlaQkBlocks : kMlaVBlocks;
+            uint64_t* full = is_k ? tail->kfull : tail->vfull;
+            uint64_t* empty = is_k ? tail->kempty : tail->vempty;
+            uint8_t* ring = is_k ? sK : sV;
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued[kAttnMaxStages] = {0, 0, 0, 0};
+            uint32_t n = 0;
+            bool ok = true;
+            for (int r = 0, i = attn_round_item(0); i < P.total_items && ok; i = attn_round_item(++r), ++n) {
+                int b, h, g, njb[2];
+                attn_item(P, i, b, h, g, njb);
+                if (is_k) {
+                    if (!mbar_wait(&tail->qempty, (n & 1) ^ 1, abort_flag, P.status)) break;
+                    mbar_arrive_expect_tx(&tail->qfull, 2 * kMlaQkBlocks * kAttnTile);
+                    for (int t = 0; t < 2; ++t)
+                        for (int c = 0; c < kMlaQkBlocks; ++c)
+                            tma_load_3d(sQ + (t * kMlaQkBlocks + c) * kAttnTile, &P.tmQ, &tail->qfull,
+                                        h * (kMlaQkBlocks * 64) + c * 64, (2 * g + t) * kAttnBlk, b);
+                }
+                const int nj = max(njb[0], njb[1]);
+                for (int j = 0; j < nj; ++j) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, P.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], nblk * kAttnTile);
+                    uint8_t* dst = ring + stage * nblk * kAttnTile;
+                    if (is_k) {
+                        tma_load_3d(dst, &P.tmK, &full[stage], h * 128, j * kAttnBlk, b);
+                        tma_load_3d(dst + kAttnTile, &P.tmK, &full[stage], h * 128 + 64, j * kAttnBlk, b);
+                        tma_load_3d(dst + 2 * kAttnTile, &P.tmKR, &full[stage], P.kr_col, j * kAttnBlk, b);
+                    } else {
+                        tma_load_3d(dst, &P.tmV, &full[stage], h * DV, j * kAttnBlk, b);
+                        tma_load_3d(dst + kAttnTile, &P.tmV, &full[stage], h * DV + 64, j * kAttnBlk, b);
+                    }
+                    ++issued[stage];
+                    if (++stage == nst) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            volatile int never = 0;
+            for (int s = 0; s < nst; ++s)
+                if (issued[s]) mbar_wait(&full[s], (issued[s] - 1) & 1, &never, P.status);
+            if (is_k && n) mbar_wait(&tail->qfull, (n - 1) & 1, &never, P.status);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        const uint32_t idesc_s = idesc_f16kind(kAttnBlk, kAttnBlk, 0, 0);  // S = Q K^T, K-major K
+        const uint32_t idesc_o = idesc_f16kind(kAttnBlk, DV, 1, 0);        // O += P V, MN-major V
+        int ks = 0, vs = 0;
+        uint32_t kph = 0, vph = 0;
+        uint32_t pc[2] = {0, 0}, no[2] = {0, 0}, n = 0;
+        bool ok = true;
+        const uint64_t qdesc0 = sw128_desc(smem_u32(sQ), 16, 1024);
+        const uint64_t kdesc0 = sw128_desc(smem_u32(sK), 16, 1024);
+        const uint64_t vdesc0 = sw128_desc(smem_u32(sV), kAttnTile, 1024);
+        const uint64_t qblk16 = (uint64_t)(kMlaQkBlocks * kAttnTile) >> 4;  // one Q tile or one K stage
+        const uint64_t vblk16 = (uint64_t)(kMlaVBlocks * kAttnTile) >> 4;   // one V stage
+        auto issue_s_tile = [&](int t) {
+            issue_s_mla(tmem_base + t * kAttnBlk, qdesc0 + (uint64_t)t * qblk16, kdesc0 + (uint64_t)ks * qblk16,
+                        idesc_s);
+            umma_commit(&tail->sfull[t]);
+        };
+        for (int r = 0, i = attn_round_item(0); i < P.total_items && ok; i = attn_round_item(++r), ++n) {
+            int b, h, g, njb[2];
+            attn_item(P, i, b, h, g, njb);
+            const int nj = max(njb[0], njb[1]);
+            if (!mbar_wait(&tail->qfull, n & 1, abort_flag, P.status)) break;
+            // S_t(0) of both tiles
+            if (!mbar_wait(&tail->kfull[ks], kph, abort_flag, P.status)) break;
+            tc_fence_after();
+            if (lane == 0) {
+#pragma unroll
+                for (int t = 0; t < 2; ++t)
+                    if (njb[t] > 0) issue_s_tile(t);
+                umma_commit(&tail->kempty[ks]);
+                if (nj == 1) umma_commit(&tail->qempty);
+            }
+            __syncwarp();
+            if (++ks == kMlaKStages) {
+                ks = 0;
+                kph ^= 1;
+            }
+            for (int j = 0; j < nj && ok; ++j) {
+                // O_t += P_t(j) V_j, then S_t(j + 1) into the columns P_t(j) occupied
+                if (!mbar_wait(&tail->vfull[vs], vph, abort_flag, P.status)) {
+                    ok = false;
+                    break;
+                }
+                const bool next_k = j + 1 < nj;
+                if (next_k && !mbar_wait(&tail->kfull[ks], kph, abort_flag, P.status)) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    if (!ok || j >= njb[t]) continue;
+                    if (j == 0 && !mbar_wait(&tail->oempty[t], (no[t] & 1) ^ 1, abort_flag, P.status)) ok = false;
+                    if (ok && !mbar_wait(&tail->pfull[t], pc[t] & 1, abort_flag, P.status)) ok = false;
+                    if (!ok) continue;
+                    tc_fence_after();
+                    if (lane == 0) {
+                        issue_pv_tmem_a(tmem_base + 256 + t * DV, tmem_base + t * kAttnBlk,
+                                        vdesc0 + (uint64_t)vs * vblk16, idesc_o, j != 0);
+                        umma_commit(&tail->oready[t]);
+                        if (j + 1 < njb[t]) issue_s_tile(t);
+                    }
+                    __syncwarp();
+                    ++pc[t];
+                    if (j == njb[t] - 1) ++no[t];
+                }
+                if (!ok) break;
+                if (lane == 0) {
+                    umma_commit(&tail->vempty[vs]);  // V_j consumed by both tiles
+                    if (next_k) {
+                        umma_commit(&tail->kempty[ks]);                // K_{j+1} consumed
+                        if (j + 1 == nj - 1) umma_commit(&tail->qempty);  // the item's last use of Q
+                    }
+                }
+                __syncwarp();
+                if (++vs == kMlaVStages) {
+                    vs = 0;
+                    vph ^= 1;
+                }
+                if (next_k && ++ks == kMlaKStages) {
+                    ks = 0;
+                    kph ^= 1;
+                }
+            }
+        }
+        if (lane == 0) umma_commit(&tail->drain);
+        __syncwarp();
+        volatile int never = 0;
+        mbar_wait(&tail->drain, 0, &never, P.status);
+    }
+    } else {
+        setmaxnreg_inc<attn_regs_high<64>()>();
+        // ---------------- softmax and output: tile t = warpgroup - 1 ----------------
+        const int t = warp >= 8 ? 1 : 0;
+        const int quarter = warp & 3;
+        const int lr = quarter * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tS = tmem_base + lane_base + t * kAttnBlk;  // S_t, and P_t over its first 64 columns
+        const uint32_t tO = tmem_base + lane_base + 256 + t * DV;
+        uint32_t sc = 0, pc = 0;
+        bool ok = true;
+        for (int r = 0, i = attn_round_item(0); i < P.total_items && ok; i = attn_round_item(++r)) {
+            int b, h, g, njb[2];
+            attn_item(P, i, b, h, g, njb);
+            const int nj = njb[t];
+            if (nj == 0) continue;
+            const int it = 2 * g + t;
+            const int row = it * kAttnBlk + lr;
+            const bool row_ok = row < P.T;
+            float m = -INFINITY, l = 0.f, m_raw = -INFINITY;
+            for (int j = 0; j < nj && ok; ++j) {
+                if (!mbar_wait(&tail->sfull[t], sc & 1, abort_flag, P.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                float v[kAttnBlk];
+                uint32_t* vu = reinterpret_cast<uint32_t*>(v);
+#pragma unroll
+                for (int c = 0; c < kAttnBlk / 32; ++c) tmem_ld32(tS + c * 32, vu + c * 32);
+                tmem_ld_wait();
+                ++sc;
+                const int key0 = j * kAttnBlk;
+                const bool full = (it + 1) * kAttnBlk <= P.T && key0 + kAttnBlk <= P.T &&
+                                  (!P.causal || key0 + kAttnBlk - 1 <= it * kAttnBlk);
+                if (!full) {
+                    const int lim = !row_ok ? 0 : (P.causal ? min(row + 1, P.T) : P.T);
+#pragma unroll
+                    for (int e = 0; e < kAttnBlk; ++e)
+                        if (key0 + e >= lim) v[e] = -INFINITY;
+                }
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int e = 0; e < kAttnBlk; e += 8)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) m4[c] = max3_nan(m4[c], v[e + 2 * c], v[e + 2 * c + 1]);
+                const float mb = max_nan(max_nan(m4[0], m4[1]), max_nan(m4[2], m4[3]));
+                m_raw = max_nan(m_raw, mb);
+                const float mx = mb * P.scale_log2;
+                const float m_new = !row_ok ? 0.f : (mx > m + 8.f || m == -INFINITY) ? fmaxf(m, mx) : m;
+                const float alpha = row_ok && m_new != m ? ex2_approx(m - m_new) : 1.f;
+                float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int e = 0; e < kAttnBlk; ++e) {
+                    const float p = row_ok ? ex2_approx(__fmaf_rn(v[e], P.scale_log2, -m_new)) : 0.f;
+                    v[e] = p;
+                    ls[e & 7] += p;
+                }
+                const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+                l = __fmaf_rn(l, alpha, lsum);
+                m = m_new;
+                if (j >= 1) {
+                    // O_t is free (and P_t(j-1) read) once P_{j-1} V_{j-1} is done
+                    if (!mbar_wait(&tail->oready[t], (pc - 1) & 1, abort_flag, P.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
+                        #pragma unroll 1
+                        for (int c = 0; c < DV / 32; ++c) {
+                            uint32_t o[32];
+                            tmem_ld32(tO + c * 32, o);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                            tmem_st32(tO + c * 32, o);
+                        }
+                    }
+                }
+                // P_t(j) as bf16 pairs over S_t's first 64 columns
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t pw[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        __nv_bfloat162 hh = __floats2bfloat162_rn(v[q4 * 32 + 2 * e], v[q4 * 32 + 2 * e + 1]);
+                        pw[e] = *reinterpret_cast<uint32_t*>(&hh);
+                    }
+                    tmem_st16(tS + q4 * 16, pw);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tail->pfull[t]);
+                ++pc;
+            }
+            if (!ok) break;
+            if (!mbar_wait(&tail->oready[t], (pc - 1) & 1, abort_flag, P.status)) break;
+            tc_fence_after();
+            const float inv = row_ok ? 1.f / l : 0.f;
+            __nv_bfloat16* orow = P.o + ((size_t)b * P.T + (row_ok ? row : 0)) * P.ld + (size_t)h * DV;
+            #pragma unroll 1
+            for (int c = 0; c < DV / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tO + c * 32, o);
+                tmem_ld_wait();
+                if (row_ok) {
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8) {
+                        __nv_bfloat162 hh[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            hh[e] = __floats2bfloat162_rn(__uint_as_float(o[q8 * 8 + 2 * e]) * inv,
+                                                          __uint_as_float(o[q8 * 8 + 2 * e + 1]) * inv);
+                        *reinterpret_cast<uint4*>(orow + c * 32 + q8 * 8) = *reinterpret_cast<uint4*>(hh);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tail->oempty[t]);
+            const float mw = warp_max_nan(row_ok ? m_raw : -INFINITY);
+            if (lane == 0 && mw != -INFINITY) atomicMax(&P.keys[b * P.H + h], float_key(mw));
+        }
+    }
+
+    pdl_trigger();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, 512);
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned old = atomicAdd(P.done, 1u);
+        tail->last_cta = old == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (tail->last_cta) {
+        __threadfence();
+        for (int h = threadIdx.x; h < P.H; h += blockDim.x)
+            finalize_head(P.keys, P.B, P.H, h, P.sqrt_d, P.accumulate, P.s_max, P.s_bh, P.status);
+    }
+}
+
+static cudaError_t launch_attn_mla(const AttnArgs& a, cudaStream_t stream) {
+    AttnParams P;
+    memset(&P, 0, sizeof(P));
+    const uint64_t q_ld = (uint64_t)a.H * 192, kv_ld = (uint64_t)a.H * 128;
+    if (!make_tmap_3d(&P.tmQ, a.q, q_ld, a.T, a.B, q_ld, q_ld * a.T, 64, kAttnBlk, 0)) return cudaErrorInvalidValue;
+    if (!make_tmap_3d(&P.tmK, a.k, kv_ld, a.T, a.B, kv_ld, kv_ld * a.T, 64, kAttnBlk, 0)) return cudaErrorInvalidValue;
+    if (!make_tmap_3d(&P.tmV, a.v, kv_ld, a.T, a.B, kv_ld, kv_ld * a.T, 64, kAttnBlk, 0)) return cudaErrorInvalidValue;
+    if (!make_tmap_3d(&P.tmKR, a.kr, (uint64_t)a.kr_ld, a.T, a.B, (uint64_t)a.kr_ld, (uint64_t)a.kr_ld * a.T, 64,
+                      kAttnBlk, 0))
+        return cudaErrorInvalidValue;
+    P.kr_col = a.kr_col;
+    P.B = a.B;
+    P.T = a.T;
+    P.H = a.H;
+    P.dh = 192;
+    P.causal = a.causal;
+    P.n_it = (a.T + kAttnBlk - 1) / kAttnBlk;
+    P.n_pair = (P.n_it + 1) / 2;
+    P.total_items = a.B * a.H * P.n_pair;
+    P.o = reinterpret_cast<__nv_bfloat16*>(a.o);
+    P.ld = (long long)kv_ld;
+    P.scale_log2 = (float)(1.4426950408889634 / sqrt(192.0));
+    P.keys = a.keys;
+    P.done = a.keys + (size_t)a.B * a.H;
+    P.sqrt_d = sqrtf(192.0f);
+    P.accumulate = a.accumulate;
+    P.s_max = a.s_max;
+    P.s_bh = a.s_bh;
+    P.status = device_status_ptr();
+    P.kst = kMlaKStages;
+    P.vst = kMlaVStages;
+    static bool attr_set[64] = {false};
+    int dev = current_device();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    if (dev < 64 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(attn_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    int grid = num_sms();
+    if (grid > P.total_items) grid = P.total_items;
+    P.band = std::max(1, std::min(a.B * a.H, (2 * grid + P.n_pair - 1) / P.n_pair));
+    TraceScope ts("attn_mla", stream);
+    return launch_pdl(attn_mla_kernel, dim3(grid), dim3(kAttnThreads), kAttnSmem, stream, P);
+}
+
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {
+    if (a.mla) return launch_attn_mla(a, stream);
     AttnParams P;
     memset(&P, 0, sizeof(P));
     if (a.dh != 64 && a.dh != 128) return cudaErrorInvalidValue;

@@ -164,10 +164,13 @@ cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream);
 
 // Attention forward with the max logit taken along (attn.cu) -------------------
 struct AttnArgs {
-    const void* q;       // bf16 [B][T][H*dh]
-    const void* k;
-    const void* v;
-    void* o;             // bf16 [B][T][H*dh]
+    const void* q;       // bf16 [B][T][H*dh]; MLA: [B][T][H*(nope+rope)], q^C then q^R per head
+    const void* k;       // MLA: k^C [B][T][H*nope]
+    const void* v;       // MLA: [B][T][H*dv]
+    const void* kr;      // MLA only: the shared k^R, rows of kr_ld elements, rope columns from kr_col
+    int kr_ld, kr_col;
+    int mla;             // 1: MLA with nope = 128, rope = 64, dv = 128 (dh = 192 for the logits)
+    void* o;             // bf16 [B][T][H*dh]; MLA: [B][T][H*dv]
     int B, T, H, dh, causal;
     unsigned* keys;      // [B*H] zeroed monotonic keys, then a zeroed done counter
     int accumulate;
