@@ -549,9 +549,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
 // Same roles and item order as attn_kernel.  S_t = Q_t K_j^T runs over three
 // 64-wide blocks: the two q^C blocks of the head against its k^C blocks and
 // the q^R block against the shared k^R (loaded from its own tensor).  Q, K
-// and V of two tiles fill shared memory (96 + 2 x 48 + 32 KB), so P_t goes
+// and V of two tiles leave no room for P in shared memory, so P_t goes
 // to TMEM, over the first 64 columns of S_t (S0 | S1 | O0 | O1 fill the 512
-// columns).  The MMA thread therefore issues S_t(j+1) only after
+// columns).  Shared memory: Q of two tiles (96 KB), one K stage (48 KB), two
+// V stages (64 KB).  The MMA thread therefore issues S_t(j+1) only after
 // O_t += P_t(j) V_j: the tensor pipe executes one thread's MMAs in issue
 // order, so the product has read P before the next S overwrites it, and the
 // softmax writes P_t(j) only after it has loaded S_t(j) and after the
@@ -571,8 +572,12 @@ MC_D void issue_s_mla(uint32_t d_tmem, uint64_t qd, uint64_t kd, uint32_t idesc)
     }
 }
 constexpr int kMlaVBlocks = 2;   // dv = 128
-constexpr int kMlaKStages = 2;
-constexpr int kMlaVStages = 1;
+// V gets the second stage: V_{j+1} must land during block j (the next P.V
+// waits on it first thing), while K_{j+1} is needed only after P_0(j) V_j
+// has been issued and can load from the end of block j - 1 (measured: one V
+// stage left the MMA thread waiting about 0.9 us for V every block)
+constexpr int kMlaKStages = 1;
+constexpr int kMlaVStages = 2;
 static_assert((2 * kMlaQkBlocks + kMlaKStages * kMlaQkBlocks + kMlaVStages * kMlaVBlocks) * kAttnTile <= kAttnRing,
               "MLA shared memory");
 
@@ -724,10 +729,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_mla_kernel(const __grid_
                     break;
                 }
                 const bool next_k = j + 1 < nj;
-                if (next_k && !mbar_wait(&tail->kfull[ks], kph, abort_flag, P.status)) {
-                    ok = false;
-                    break;
-                }
+                bool have_k = false;  // K_{j+1} landed: waited for just before its first use
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     if (!ok || j >= njb[t]) continue;
@@ -739,9 +741,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_mla_kernel(const __grid_
                         issue_pv_tmem_a(tmem_base + 256 + t * DV, tmem_base + t * kAttnBlk,
                                         vdesc0 + (uint64_t)vs * vblk16, idesc_o, j != 0);
                         umma_commit(&tail->oready[t]);
-                        if (j + 1 < njb[t]) issue_s_tile(t);
                     }
                     __syncwarp();
+                    if (j + 1 < njb[t]) {
+                        if (!have_k) {
+                            if (!mbar_wait(&tail->kfull[ks], kph, abort_flag, P.status)) {
+                                ok = false;
+                                continue;
+                            }
+                            tc_fence_after();
+                            have_k = true;
+                        }
+                        if (lane == 0) issue_s_tile(t);
+                        __syncwarp();
+                    }
                     ++pc[t];
                     if (j == njb[t] - 1) ++no[t];
                 }
