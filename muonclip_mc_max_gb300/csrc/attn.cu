@@ -428,14 +428,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                 const float mx = mb * P.scale_log2;
                 const float m_new = !row_ok ? 0.f : (mx > m + 8.f || m == -INFINITY) ? fmaxf(m, mx) : m;
                 const float alpha = row_ok && m_new != m ? ex2_approx(m - m_new) : 1.f;
-                float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // eight partial sums
+                // pairs of logits through the packed fp32 FMA and add of
+                // sm_100+; logit e goes to partial sum e mod 8
+                const float2 sc2 = make_float2(P.scale_log2, P.scale_log2), nm2 = make_float2(-m_new, -m_new);
+                float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                make_float2(0.f, 0.f)};
 #pragma unroll
-                for (int e = 0; e < kAttnBlk; ++e) {
-                    const float p = row_ok ? ex2_approx(__fmaf_rn(v[e], P.scale_log2, -m_new)) : 0.f;
-                    v[e] = p;
-                    ls[e & 7] += p;
+                for (int e = 0; e < kAttnBlk; e += 2) {
+                    const float2 x = __ffma2_rn(make_float2(v[e], v[e + 1]), sc2, nm2);
+                    const float p0 = row_ok ? ex2_approx(x.x) : 0.f, p1 = row_ok ? ex2_approx(x.y) : 0.f;
+                    v[e] = p0;
+                    v[e + 1] = p1;
+                    ls[(e >> 1) & 3] = __fadd2_rn(ls[(e >> 1) & 3], make_float2(p0, p1));
                 }
-                const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+                const float lsum = ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) + ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
                 l = __fmaf_rn(l, alpha, lsum);
                 m = m_new;
                 if (j >= 1) {
@@ -833,14 +839,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_mla_kernel(const __grid_
                 const float mx = mb * P.scale_log2;
                 const float m_new = !row_ok ? 0.f : (mx > m + 8.f || m == -INFINITY) ? fmaxf(m, mx) : m;
                 const float alpha = row_ok && m_new != m ? ex2_approx(m - m_new) : 1.f;
-                float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                // pairs of logits through the packed fp32 FMA and add of
+                // sm_100+; logit e goes to partial sum e mod 8
+                const float2 sc2 = make_float2(P.scale_log2, P.scale_log2), nm2 = make_float2(-m_new, -m_new);
+                float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                make_float2(0.f, 0.f)};
 #pragma unroll
-                for (int e = 0; e < kAttnBlk; ++e) {
-                    const float p = row_ok ? ex2_approx(__fmaf_rn(v[e], P.scale_log2, -m_new)) : 0.f;
-                    v[e] = p;
-                    ls[e & 7] += p;
+                for (int e = 0; e < kAttnBlk; e += 2) {
+                    const float2 x = __ffma2_rn(make_float2(v[e], v[e + 1]), sc2, nm2);
+                    const float p0 = row_ok ? ex2_approx(x.x) : 0.f, p1 = row_ok ? ex2_approx(x.y) : 0.f;
+                    v[e] = p0;
+                    v[e + 1] = p1;
+                    ls[(e >> 1) & 3] = __fadd2_rn(ls[(e >> 1) & 3], make_float2(p0, p1));
                 }
-                const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+                const float lsum = ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) + ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
                 l = __fmaf_rn(l, alpha, lsum);
                 m = m_new;
                 if (j >= 1) {
