@@ -430,13 +430,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                 const float alpha = row_ok && m_new != m ? ex2_approx(m - m_new) : 1.f;
                 // pairs of logits through the packed fp32 FMA and add of
                 // sm_100+; logit e goes to partial sum e mod 8
-                const float2 sc2 = make_float2(P.scale_log2, P.scale_log2), nm2 = make_float2(-m_new, -m_new);
+                // (at dh = 128 rows past the sequence subtract -inf, so their
+                // weights are 0 with no select; at dh = 64 the selects keep
+                // the register allocation free of spills)
+                const float nm = (DH == 128 && !row_ok) ? -INFINITY : -m_new;
+                const float2 sc2 = make_float2(P.scale_log2, P.scale_log2), nm2 = make_float2(nm, nm);
                 float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                 make_float2(0.f, 0.f)};
 #pragma unroll
                 for (int e = 0; e < kAttnBlk; e += 2) {
                     const float2 x = __ffma2_rn(make_float2(v[e], v[e + 1]), sc2, nm2);
-                    const float p0 = row_ok ? ex2_approx(x.x) : 0.f, p1 = row_ok ? ex2_approx(x.y) : 0.f;
+                    const bool keep = DH == 128 || row_ok;
+                    const float p0 = keep ? ex2_approx(x.x) : 0.f, p1 = keep ? ex2_approx(x.y) : 0.f;
                     v[e] = p0;
                     v[e + 1] = p1;
                     ls[(e >> 1) & 3] = __fadd2_rn(ls[(e >> 1) & 3], make_float2(p0, p1));
