@@ -339,6 +339,10 @@ MC_D void chunk_values(const GemmProblem& q, int row0, int col0, float* f, float
 #pragma unroll
         for (int it = 0; it < 8; ++it) *reinterpret_cast<uint4*>(S + stage_off(swz, it * 4 + sub, seg)) = u[it];
         __syncwarp();
+        // v = sc (alpha acc + beta aux), pairs of values through the packed
+        // fp32 arithmetic of sm_100+: beta aux, then one fused multiply-add,
+        // then the scale, each rounded once
+        const float2 al2 = make_float2(alpha, alpha), be2 = make_float2(beta, beta), sc2 = make_float2(sc, sc);
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
             uint4 w = *reinterpret_cast<const uint4*>(S + stage_off(swz, lane, v));
@@ -348,15 +352,22 @@ MC_D void chunk_values(const GemmProblem& q, int row0, int col0, float* f, float
             for (int i = 0; i < 4; ++i) {
                 // aux has the operands' type (fp16 or bf16)
                 const float2 a2 = aux_f16 ? __half22float2(hf[i]) : __bfloat1622float2(h[i]);
-                f[8 * v + 2 * i] = sc * (alpha * f[8 * v + 2 * i] + beta * a2.x);
-                f[8 * v + 2 * i + 1] = sc * (alpha * f[8 * v + 2 * i + 1] + beta * a2.y);
+                const float2 acc = make_float2(f[8 * v + 2 * i], f[8 * v + 2 * i + 1]);
+                const float2 r = __fmul2_rn(sc2, __ffma2_rn(al2, acc, __fmul2_rn(be2, a2)));
+                f[8 * v + 2 * i] = r.x;
+                f[8 * v + 2 * i + 1] = r.y;
             }
         }
         __syncwarp();
     } else if (q.alpha != 1.0f || sc != 1.0f) {
-        const float s2 = sc * q.alpha;
+        const float s = sc * q.alpha;
+        const float2 s2 = make_float2(s, s);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) f[i] *= s2;
+        for (int i = 0; i < 64; i += 2) {
+            const float2 r = __fmul2_rn(s2, make_float2(f[i], f[i + 1]));
+            f[i] = r.x;
+            f[i + 1] = r.y;
+        }
     }
 }
 
