@@ -4,6 +4,9 @@
 // max logit of this step and leaves the forward unchanged) costs one max per
 // logit on top of O = softmax(Q K^T / sqrt(dh)) V.
 //
+// This kernel runs dh = 64; dh = 128 runs on the MLA kernel below with two
+// 64-wide blocks per logit (P over the S columns in TMEM).
+//
 // Work item = (sequence b, head h, pair of 128-query tiles); one persistent
 // CTA per SM; items in bands of (b, h) pairs dealt in snake-ordered rounds
 // (as in the scan).  Per 128-key block j of an item:
@@ -13,8 +16,7 @@
 //   warp 1      tcgen05.mma S_t = Q_t K_j^T for both tiles into two
 //               128 x 128 fp32 TMEM tiles; once P_t is ready, O_t += P_t V
 //               into the tile's 128 x dh fp32 TMEM accumulator (V MN-major
-//               as stored; P_t from TMEM at dh = 64, from shared memory at
-//               dh = 128)
+//               as stored; P_t from TMEM)
 //   warpgroups 1, 2   one query row per thread of tile 0 / tile 1: S_t from
 //               TMEM, the raw row max (for S_max), the running softmax max m
 //               and sum l, O_t rescaled in TMEM when m moves, P_t = 2^(s - m)
@@ -32,23 +34,18 @@ namespace mc {
 //   warpgroup 1  softmax and output of query tile 0 (one row per thread)
 //   warpgroup 2  softmax and output of query tile 1
 // Registers move from warpgroup 0 to the softmax warpgroups with setmaxnreg
-// (dh = 128: 128 x 120 + 256 x 184 = 62464; dh = 64, where the softmax also
-// packs P for TMEM: 128 x 96 + 256 x 200 = 63488; both <= 384 threads x 168
-// at launch); each warpgroup's branch starts with its setmaxnreg, so the
-// compiler allocates the softmax code with the larger budget (128 logits per
-// thread stay in registers).
+// (128 x 96 + 256 x 200 = 63488 <= 384 threads x 168 at launch); each
+// warpgroup's branch starts with its setmaxnreg, so the compiler allocates
+// the softmax code with the larger budget (128 logits per thread stay in
+// registers, and P is packed for TMEM).
 constexpr int kAttnThreads = 384;
-template <int DH>
-__host__ __device__ constexpr int attn_regs_low() { return DH == 64 ? 96 : 120; }
-template <int DH>
-__host__ __device__ constexpr int attn_regs_high() { return DH == 64 ? 200 : 184; }
-static_assert(128 * attn_regs_low<64>() + 256 * attn_regs_high<64>() <= kAttnThreads * (65536 / kAttnThreads / 8 * 8) &&
-                  128 * attn_regs_low<128>() + 256 * attn_regs_high<128>() <= kAttnThreads * (65536 / kAttnThreads / 8 * 8),
+constexpr int kAttnRegsLow = 96, kAttnRegsHigh = 200;
+static_assert(128 * kAttnRegsLow + 256 * kAttnRegsHigh <= kAttnThreads * (65536 / kAttnThreads / 8 * 8),
               "register split");
 constexpr int kAttnBlk = 128;          // queries per tile, keys per key block
 constexpr int kAttnMaxStages = 4;
 constexpr int kAttnTile = 16384;       // 128 rows x 64 bf16 (one 128-byte-swizzled block)
-constexpr int kAttnRing = 224 * 1024;  // Q and P of two tiles, then the K and V rings
+constexpr int kAttnRing = 224 * 1024;  // Q of two tiles, then the K and V rings
 constexpr int kAttnSmem = 1024 + 1024 + kAttnRing;
 
 struct AttnParams {
@@ -122,26 +119,15 @@ MC_D int attn_round_item(int r) {
 // The MMA warp shares its SM sub-partition with two softmax warps, so its
 // issue path is kept short: descriptors are formed once per tile or stage
 // and a K step only adds a constant to the 16-byte address field.
-// S_t = Q_t K^T: K-major Q and K, nc 64-wide blocks of 4 steps each.
-template <int NC>
+// S_t = Q_t K^T at dh = 64: K-major Q and K, one 64-wide block, 4 steps
 MC_D void issue_s(uint32_t d_tmem, uint64_t qd, uint64_t kd, uint32_t idesc) {
 #pragma unroll
-    for (int k = 0; k < 4 * NC; ++k) {
-        const uint64_t off = (uint64_t)(((k >> 2) * kAttnTile + (k & 3) * 32) >> 4);
-        umma_bf16(d_tmem, qd + off, kd + off, idesc, k != 0);
-    }
-}
-// O_t (+)= P_t V: P K-major (two 64-key blocks), V MN-major (2 KB per K step)
-MC_D void issue_pv(uint32_t d_tmem, uint64_t pd, uint64_t vd, uint32_t idesc, bool acc) {
-#pragma unroll
-    for (int k = 0; k < kAttnBlk / 16; ++k) {
-        const uint64_t aoff = (uint64_t)(((k >> 2) * kAttnTile + (k & 3) * 32) >> 4);
-        umma_bf16(d_tmem, pd + aoff, vd + (uint64_t)(k * (2048 >> 4)), idesc, acc || k != 0);
-    }
+    for (int k = 0; k < 4; ++k) umma_bf16(d_tmem, qd + (uint64_t)(k * 2), kd + (uint64_t)(k * 2), idesc, k != 0);
 }
 
-// dh = 64: P_t in TMEM (one row per lane, two bf16 keys per 32-bit column,
-// 64 columns for 128 keys) as the A operand, 8 columns per K step
+// O_t (+)= P_t V with P_t in TMEM (one row per lane, two bf16 keys per
+// 32-bit column, 64 columns for 128 keys) as the A operand, 8 columns per
+// K step; V MN-major (2 KB per K step)
 MC_D void issue_pv_tmem_a(uint32_t d_tmem, uint32_t p_tmem, uint64_t vd, uint32_t idesc, bool acc) {
 #pragma unroll
     for (int k = 0; k < kAttnBlk / 16; ++k) {
@@ -158,21 +144,19 @@ MC_D void setmaxnreg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" 
 template <uint32_t N>
 MC_D void setmaxnreg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
 
-template <int DH>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_constant__ AttnParams P) {
+    constexpr int DH = 64;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     static_assert(sizeof(AttnSmemTail) <= 1024, "tail");
     AttnSmemTail* tail = reinterpret_cast<AttnSmemTail*>(smem);
-    const int nc = DH / 64;                 // 64-column blocks per row of q, k, v
-    uint8_t* sQ = smem + 1024;                // tile t: blocks t*nc ..
-    uint8_t* sP = sQ + 2 * nc * kAttnTile;    // tile t: 2 blocks (128 keys) at sP + 2t blocks
-    uint8_t* sK = sP + 4 * kAttnTile;         // stage s: nc blocks
-    uint8_t* sV = sK + P.kst * nc * kAttnTile;
+    uint8_t* sQ = smem + 1024;             // tile t: block t
+    uint8_t* sK = sQ + 2 * kAttnTile;      // stage s: one block
+    uint8_t* sV = sK + P.kst * kAttnTile;
     volatile int* abort_flag = &tail->abort_flag;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t blk_bytes = (uint32_t)(nc * kAttnTile);
+    const uint32_t blk_bytes = (uint32_t)kAttnTile;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kAttnMaxStages; ++s) {
@@ -210,7 +194,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     pdl_wait();
 
     if (warp < 4) {
-    setmaxnreg_dec<attn_regs_low<DH>()>();
+    setmaxnreg_dec<kAttnRegsLow>();
     if (warp == 0 || warp == 2) {
         // ---------------- TMA producers: Q and K (warp 0), V (warp 2) ----------------
         if (lane == 0) {
@@ -233,9 +217,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                     if (!mbar_wait(&tail->qempty, (n & 1) ^ 1, abort_flag, P.status)) break;
                     mbar_arrive_expect_tx(&tail->qfull, 2 * blk_bytes);
                     for (int t = 0; t < 2; ++t)
-                        for (int c = 0; c < nc; ++c)
-                            tma_load_3d(sQ + (t * nc + c) * kAttnTile, &P.tmQ, &tail->qfull, h * DH + c * 64,
-                                        (2 * g + t) * kAttnBlk, b);
+                        tma_load_3d(sQ + t * kAttnTile, &P.tmQ, &tail->qfull, h * DH, (2 * g + t) * kAttnBlk, b);
                 }
                 const int nj = max(njb[0], njb[1]);
                 for (int j = 0; j < nj; ++j) {
@@ -244,9 +226,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                         break;
                     }
                     mbar_arrive_expect_tx(&full[stage], blk_bytes);
-                    for (int c = 0; c < nc; ++c)
-                        tma_load_3d(ring + (stage * nc + c) * kAttnTile, tm, &full[stage], h * DH + c * 64,
-                                    j * kAttnBlk, b);
+                    tma_load_3d(ring + stage * kAttnTile, tm, &full[stage], h * DH, j * kAttnBlk, b);
                     ++issued[stage];
                     if (++stage == nst) {
                         stage = 0;
@@ -272,10 +252,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         // descriptors of tile 0 / ring stage 0; tile 1 and stage s add a
         // multiple of the block size (in 16-byte units) to the address field
         const uint64_t qdesc0 = sw128_desc(smem_u32(sQ), 16, 1024);
-        const uint64_t pdesc0 = sw128_desc(smem_u32(sP), 16, 1024);
         const uint64_t kdesc0 = sw128_desc(smem_u32(sK), 16, 1024);
         const uint64_t vdesc0 = sw128_desc(smem_u32(sV), kAttnTile, 1024);
-        const uint64_t blk16 = (uint64_t)(nc * kAttnTile) >> 4;  // one stage or one Q tile
+        const uint64_t blk16 = (uint64_t)kAttnTile >> 4;  // one stage or one Q tile
         // O_t += P_t V_jj for both tiles that use key block jj; the first
         // product of an item overwrites O_t once the previous output is read
         // Each pair of products waits for both tiles' barriers first and is
@@ -293,12 +272,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
             if (lane == 0) {
                 for (int t = 0; t < 2; ++t) {
                     if (jj >= njb[t]) continue;
-                    if (nc == 1)  // P_t in TMEM after O0 and O1
-                        issue_pv_tmem_a(tmem_base + 256 + t * DH, tmem_base + 256 + 2 * DH + t * (kAttnBlk / 2),
-                                        vdesc0 + (uint64_t)vs * blk16, idesc_o, jj != 0);
-                    else
-                        issue_pv(tmem_base + 256 + t * DH, pdesc0 + (uint64_t)(t * ((2 * kAttnTile) >> 4)),
-                                 vdesc0 + (uint64_t)vs * blk16, idesc_o, jj != 0);
+                    // P_t in TMEM after O0 and O1
+                    issue_pv_tmem_a(tmem_base + 256 + t * DH, tmem_base + 256 + 2 * DH + t * (kAttnBlk / 2),
+                                    vdesc0 + (uint64_t)vs * blk16, idesc_o, jj != 0);
                     umma_commit(&tail->oready[t]);
                 }
                 umma_commit(&tail->vempty[vs]);  // V_jj consumed by both tiles
@@ -336,10 +312,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                     for (int t = 0; t < 2; ++t) {
                         if (j >= njb[t]) continue;
                         const uint64_t qd = qdesc0 + (uint64_t)t * blk16, kd = kdesc0 + (uint64_t)ks * blk16;
-                        if (nc == 1)
-                            issue_s<1>(tmem_base + t * kAttnBlk, qd, kd, idesc_s);
-                        else
-                            issue_s<2>(tmem_base + t * kAttnBlk, qd, kd, idesc_s);
+                        issue_s(tmem_base + t * kAttnBlk, qd, kd, idesc_s);
                         umma_commit(&tail->sfull[t]);
                     }
                     umma_commit(&tail->kempty[ks]);                // K_j consumed
@@ -367,7 +340,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         mbar_wait(&tail->drain, 0, &never, P.status);
     }
     } else {
-        setmaxnreg_inc<attn_regs_high<DH>()>();
+        setmaxnreg_inc<kAttnRegsHigh>();
         // ---------------- softmax and output: tile t = warpgroup - 1 ----------------
         const int t = warp >= 8 ? 1 : 0;
         const int quarter = warp & 3;        // TMEM lanes 32 q .. 32 q + 31
@@ -375,8 +348,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         const uint32_t tS = tmem_base + lane_base + t * kAttnBlk;
         const uint32_t tO = tmem_base + lane_base + 256 + t * DH;
-        const uint32_t tP = tmem_base + lane_base + 256 + 2 * DH + t * (kAttnBlk / 2);  // dh = 64 only
-        uint8_t* pt = sP + 2 * t * kAttnTile;
+        const uint32_t tP = tmem_base + lane_base + 256 + 2 * DH + t * (kAttnBlk / 2);
         uint32_t sc = 0, pc = 0;
         bool ok = true;
         for (int r = 0, i = attn_round_item(0); i < P.total_items && ok; i = attn_round_item(++r)) {
@@ -430,18 +402,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                 const float alpha = row_ok && m_new != m ? ex2_approx(m - m_new) : 1.f;
                 // pairs of logits through the packed fp32 FMA and add of
                 // sm_100+; logit e goes to partial sum e mod 8
-                // (at dh = 128 rows past the sequence subtract -inf, so their
-                // weights are 0 with no select; at dh = 64 the selects keep
-                // the register allocation free of spills)
-                const float nm = (DH == 128 && !row_ok) ? -INFINITY : -m_new;
-                const float2 sc2 = make_float2(P.scale_log2, P.scale_log2), nm2 = make_float2(nm, nm);
+                const float2 sc2 = make_float2(P.scale_log2, P.scale_log2), nm2 = make_float2(-m_new, -m_new);
                 float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                 make_float2(0.f, 0.f)};
 #pragma unroll
                 for (int e = 0; e < kAttnBlk; e += 2) {
                     const float2 x = __ffma2_rn(make_float2(v[e], v[e + 1]), sc2, nm2);
-                    const bool keep = DH == 128 || row_ok;
-                    const float p0 = keep ? ex2_approx(x.x) : 0.f, p1 = keep ? ex2_approx(x.y) : 0.f;
+                    const float p0 = row_ok ? ex2_approx(x.x) : 0.f, p1 = row_ok ? ex2_approx(x.y) : 0.f;
                     v[e] = p0;
                     v[e + 1] = p1;
                     ls[(e >> 1) & 3] = __fadd2_rn(ls[(e >> 1) & 3], make_float2(p0, p1));
@@ -469,32 +436,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                         tmem_st_wait();
                     }
                 }
-                if constexpr (DH == 64) {
-                    // P_j as bf16 pairs into this row's 64 TMEM columns (the A
-                    // operand of P.V; TMEM holds S, O and P of both tiles at dh = 64)
+                // P_j as bf16 pairs into this row's 64 TMEM columns (the A
+                // operand of P.V; TMEM holds S, O and P of both tiles)
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint32_t pw[16];
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t pw[16];
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            __nv_bfloat162 hh = __floats2bfloat162_rn(v[q4 * 32 + 2 * e], v[q4 * 32 + 2 * e + 1]);
-                            pw[e] = *reinterpret_cast<uint32_t*>(&hh);
-                        }
-                        tmem_st16(tP + q4 * 16, pw);
+                    for (int e = 0; e < 16; ++e) {
+                        __nv_bfloat162 hh = __floats2bfloat162_rn(v[q4 * 32 + 2 * e], v[q4 * 32 + 2 * e + 1]);
+                        pw[e] = *reinterpret_cast<uint32_t*>(&hh);
                     }
-                    tmem_st_wait();
-                } else {
-                    // P_j as bf16, 128-byte swizzled K-major rows (two 64-key blocks)
-#pragma unroll
-                    for (int cc = 0; cc < kAttnBlk / 8; ++cc) {
-                        __nv_bfloat162 hh[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) hh[e] = __floats2bfloat162_rn(v[cc * 8 + 2 * e], v[cc * 8 + 2 * e + 1]);
-                        *reinterpret_cast<uint4*>(pt + (cc >> 3) * kAttnTile + lr * 128 + (((cc & 7) ^ (lr & 7)) << 4)) =
-                            *reinterpret_cast<uint4*>(hh);
-                    }
-                    fence_proxy_async_smem();
+                    tmem_st16(tP + q4 * 16, pw);
                 }
+                tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tail->pfull[t]);
@@ -555,27 +509,30 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
 // MLA attention forward with the max logit taken along (K2's attention: the
 // K2 review's MLA table).  Per head the logit is q^C.k^C over nope = 128
 // plus q^R.k^R over rope = 64 with the k^R every head shares, d = 192; the
-// values and the output have dv = 128.
+// values and the output have dv = 128.  The same kernel with NQK = 2 (no
+// rope block) is the MHA forward at dh = 128.
 //
-// Same roles and item order as attn_kernel.  S_t = Q_t K_j^T runs over three
-// 64-wide blocks: the two q^C blocks of the head against its k^C blocks and
-// the q^R block against the shared k^R (loaded from its own tensor).  Q, K
-// and V of two tiles leave no room for P in shared memory, so P_t goes
-// to TMEM, over the first 64 columns of S_t (S0 | S1 | O0 | O1 fill the 512
-// columns).  Shared memory: Q of two tiles (96 KB), one K stage (48 KB), two
-// V stages (64 KB).  The MMA thread therefore issues S_t(j+1) only after
-// O_t += P_t(j) V_j: the tensor pipe executes one thread's MMAs in issue
-// order, so the product has read P before the next S overwrites it, and the
-// softmax writes P_t(j) only after it has loaded S_t(j) and after the
-// previous product (oready) has read P_t(j-1).
+// Same roles and item order as attn_kernel.  S_t = Q_t K_j^T runs over NQK
+// 64-wide blocks: for MLA the two q^C blocks of the head against its k^C
+// blocks and the q^R block against the shared k^R (loaded from its own
+// tensor).  P_t goes to TMEM, over the first 64 columns of S_t (S0 | S1 |
+// O0 | O1 fill the 512 columns), so shared memory holds only Q of two
+// tiles, the K stages and two V stages (MLA: 96 + 48 + 64 KB; dh = 128:
+// 64 + 2 x 32 + 64 KB), and no P tile is written to or read from it.  The
+// MMA thread therefore issues S_t(j+1) only after O_t += P_t(j) V_j: the
+// tensor pipe executes one thread's MMAs in issue order, so the product has
+// read P before the next S overwrites it, and the softmax writes P_t(j) only
+// after it has loaded S_t(j) and after the previous product (oready) has
+// read P_t(j-1).
 // ---------------------------------------------------------------------------
 constexpr int kMlaQkBlocks = 3;  // q^C (2 blocks) and q^R (1 block) per head
 
-// S_t = Q_t K^T over the three 64-wide blocks, the blocks in a rolled loop:
+// S_t = Q_t K^T over the NQK 64-wide blocks, the blocks in a rolled loop:
 // the MMA warp runs on the smallest register share of the kernel
+template <int NQK>
 MC_D void issue_s_mla(uint32_t d_tmem, uint64_t qd, uint64_t kd, uint32_t idesc) {
 #pragma unroll 1
-    for (int c = 0; c < kMlaQkBlocks; ++c) {
+    for (int c = 0; c < NQK; ++c) {
         const uint64_t boff = (uint64_t)((c * kAttnTile) >> 4);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
@@ -583,23 +540,28 @@ MC_D void issue_s_mla(uint32_t d_tmem, uint64_t qd, uint64_t kd, uint32_t idesc)
     }
 }
 constexpr int kMlaVBlocks = 2;   // dv = 128
-// V gets the second stage: V_{j+1} must land during block j (the next P.V
-// waits on it first thing), while K_{j+1} is needed only after P_0(j) V_j
-// has been issued and can load from the end of block j - 1 (measured: one V
-// stage left the MMA thread waiting about 0.9 us for V every block)
-constexpr int kMlaKStages = 1;
+// V gets two stages: V_{j+1} must land during block j (the next P.V waits
+// on it first thing), while K_{j+1} is needed only after P_0(j) V_j has been
+// issued and can load from the end of block j - 1 (measured: one V stage
+// left the MMA thread waiting about 0.9 us for V every block).  MLA has room
+// for one K stage, dh = 128 for two.
+template <int NQK>
+__host__ __device__ constexpr int mla_k_stages() { return NQK == kMlaQkBlocks ? 1 : 2; }
 constexpr int kMlaVStages = 2;
-static_assert((2 * kMlaQkBlocks + kMlaKStages * kMlaQkBlocks + kMlaVStages * kMlaVBlocks) * kAttnTile <= kAttnRing,
+static_assert((2 * kMlaQkBlocks + 1 * kMlaQkBlocks + kMlaVStages * kMlaVBlocks) * kAttnTile <= kAttnRing &&
+                  (2 * 2 + 2 * 2 + kMlaVStages * kMlaVBlocks) * kAttnTile <= kAttnRing,
               "MLA shared memory");
 
+template <int NQK>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_mla_kernel(const __grid_constant__ AttnParams P) {
     constexpr int DV = 128;
+    constexpr int kMlaKStages = mla_k_stages<NQK>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     AttnSmemTail* tail = reinterpret_cast<AttnSmemTail*>(smem);
-    uint8_t* sQ = smem + 1024;                                  // tile t: blocks 3t ..
-    uint8_t* sK = sQ + 2 * kMlaQkBlocks * kAttnTile;           // stage s: 3 blocks (k^C, k^C, k^R)
-    uint8_t* sV = sK + kMlaKStages * kMlaQkBlocks * kAttnTile;  // stage s: 2 blocks
+    uint8_t* sQ = smem + 1024;                          // tile t: blocks NQK t ..
+    uint8_t* sK = sQ + 2 * NQK * kAttnTile;            // stage s: NQK blocks (k^C, k^C[, k^R])
+    uint8_t* sV = sK + kMlaKStages * NQK * kAttnTile;  // stage s: 2 blocks
     volatile int* abort_flag = &tail->abort_flag;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -627,7 +589,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_mla_kernel(const __grid_
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&P.tmQ);
         tma_prefetch_desc(&P.tmK);
-        tma_prefetch_desc(&P.tmKR);
+        if (NQK == kMlaQkBlocks) tma_prefetch_desc(&P.tmKR);
         tma_prefetch_desc(&P.tmV);
     }
     if (warp == 1) {
@@ -641,13 +603,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_mla_kernel(const __grid_
     pdl_wait();
 
     if (warp < 4) {
-    setmaxnreg_dec<attn_regs_low<64>()>();  // the dh = 64 split: P goes to TMEM here too
+    setmaxnreg_dec<kAttnRegsLow>();  // the dh = 64 split: P goes to TMEM here too
     if (warp == 0 || warp == 2) {
         // ---------------- TMA producers: Q and K (warp 0), V (warp 2) ----------------
         if (lane == 0) {
             const bool is_k = warp == 0;
             const int nst = is_k ? kMlaKStages : kMlaVStages;
-            const int nblk = is_k ? kMlaQkBlocks : kMlaVBlocks;
+            const int nblk = is_k ? NQK : kMlaVBlocks;
             uint64_t* full = is_k ? tail->kfull : tail->vfull;
             uint64_t* empty = is_k ? tail->kempty : tail->vempty;
             uint8_t* ring = is_k ? sK : sV;
@@ -661,11 +623,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_mla_kernel(const __grid_
                 attn_item(P, i, b, h, g, njb);
                 if (is_k) {
                     if (!mbar_wait(&tail->qempty, (n & 1) ^ 1, abort_flag, P.status)) break;
-                    mbar_arrive_expect_tx(&tail->qfull, 2 * kMlaQkBlocks * kAttnTile);
+                    mbar_arrive_expect_tx(&tail->qfull, 2 * NQK * kAttnTile);
                     for (int t = 0; t < 2; ++t)
-                        for (int c = 0; c < kMlaQkBlocks; ++c)
-                            tma_load_3d(sQ + (t * kMlaQkBlocks + c) * kAttnTile, &P.tmQ, &tail->qfull,
-                                        h * (kMlaQkBlocks * 64) + c * 64, (2 * g + t) * kAttnBlk, b);
+                        for (int c = 0; c < NQK; ++c)
+                            tma_load_3d(sQ + (t * NQK + c) * kAttnTile, &P.tmQ, &tail->qfull,
+                                        h * (NQK * 64) + c * 64, (2 * g + t) * kAttnBlk, b);
                 }
                 const int nj = max(njb[0], njb[1]);
                 for (int j = 0; j < nj; ++j) {
@@ -678,7 +640,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_mla_kernel(const __grid_
                     if (is_k) {
                         tma_load_3d(dst, &P.tmK, &full[stage], h * 128, j * kAttnBlk, b);
                         tma_load_3d(dst + kAttnTile, &P.tmK, &full[stage], h * 128 + 64, j * kAttnBlk, b);
-                        tma_load_3d(dst + 2 * kAttnTile, &P.tmKR, &full[stage], P.kr_col, j * kAttnBlk, b);
+                        if (NQK == kMlaQkBlocks)
+                            tma_load_3d(dst + 2 * kAttnTile, &P.tmKR, &full[stage], P.kr_col, j * kAttnBlk, b);
                     } else {
                         tma_load_3d(dst, &P.tmV, &full[stage], h * DV, j * kAttnBlk, b);
                         tma_load_3d(dst + kAttnTile, &P.tmV, &full[stage], h * DV + 64, j * kAttnBlk, b);
@@ -706,10 +669,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_mla_kernel(const __grid_
         const uint64_t qdesc0 = sw128_desc(smem_u32(sQ), 16, 1024);
         const uint64_t kdesc0 = sw128_desc(smem_u32(sK), 16, 1024);
         const uint64_t vdesc0 = sw128_desc(smem_u32(sV), kAttnTile, 1024);
-        const uint64_t qblk16 = (uint64_t)(kMlaQkBlocks * kAttnTile) >> 4;  // one Q tile or one K stage
+        const uint64_t qblk16 = (uint64_t)(NQK * kAttnTile) >> 4;  // one Q tile or one K stage
         const uint64_t vblk16 = (uint64_t)(kMlaVBlocks * kAttnTile) >> 4;   // one V stage
         auto issue_s_tile = [&](int t) {
-            issue_s_mla(tmem_base + t * kAttnBlk, qdesc0 + (uint64_t)t * qblk16, kdesc0 + (uint64_t)ks * qblk16,
+            issue_s_mla<NQK>(tmem_base + t * kAttnBlk, qdesc0 + (uint64_t)t * qblk16, kdesc0 + (uint64_t)ks * qblk16,
                         idesc_s);
             umma_commit(&tail->sfull[t]);
         };
@@ -794,7 +757,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_mla_kernel(const __grid_
         mbar_wait(&tail->drain, 0, &never, P.status);
     }
     } else {
-        setmaxnreg_inc<attn_regs_high<64>()>();
+        setmaxnreg_inc<kAttnRegsHigh>();
         // ---------------- softmax and output: tile t = warpgroup - 1 ----------------
         const int t = warp >= 8 ? 1 : 0;
         const int quarter = warp & 3;
@@ -944,57 +907,67 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_mla_kernel(const __grid_
     }
 }
 
-static cudaError_t launch_attn_mla(const AttnArgs& a, cudaStream_t stream) {
+// The P-in-TMEM kernel: MLA (d = 192 over q^C, k^C and the shared k^R) or,
+// with NQK = 2, MHA at dh = 128.
+template <int NQK>
+static cudaError_t launch_attn_tmem_p(const AttnArgs& a, cudaStream_t stream) {
     AttnParams P;
     memset(&P, 0, sizeof(P));
-    const uint64_t q_ld = (uint64_t)a.H * 192, kv_ld = (uint64_t)a.H * 128;
+    constexpr int d = NQK * 64;
+    const uint64_t q_ld = (uint64_t)a.H * d, kv_ld = (uint64_t)a.H * 128;
     if (!make_tmap_3d(&P.tmQ, a.q, q_ld, a.T, a.B, q_ld, q_ld * a.T, 64, kAttnBlk, 0)) return cudaErrorInvalidValue;
     if (!make_tmap_3d(&P.tmK, a.k, kv_ld, a.T, a.B, kv_ld, kv_ld * a.T, 64, kAttnBlk, 0)) return cudaErrorInvalidValue;
     if (!make_tmap_3d(&P.tmV, a.v, kv_ld, a.T, a.B, kv_ld, kv_ld * a.T, 64, kAttnBlk, 0)) return cudaErrorInvalidValue;
-    if (!make_tmap_3d(&P.tmKR, a.kr, (uint64_t)a.kr_ld, a.T, a.B, (uint64_t)a.kr_ld, (uint64_t)a.kr_ld * a.T, 64,
-                      kAttnBlk, 0))
-        return cudaErrorInvalidValue;
-    P.kr_col = a.kr_col;
+    if (NQK == kMlaQkBlocks) {
+        if (!make_tmap_3d(&P.tmKR, a.kr, (uint64_t)a.kr_ld, a.T, a.B, (uint64_t)a.kr_ld, (uint64_t)a.kr_ld * a.T, 64,
+                          kAttnBlk, 0))
+            return cudaErrorInvalidValue;
+        P.kr_col = a.kr_col;
+    } else {
+        P.tmKR = P.tmK;  // not read
+    }
     P.B = a.B;
     P.T = a.T;
     P.H = a.H;
-    P.dh = 192;
+    P.dh = d;
     P.causal = a.causal;
     P.n_it = (a.T + kAttnBlk - 1) / kAttnBlk;
     P.n_pair = (P.n_it + 1) / 2;
     P.total_items = a.B * a.H * P.n_pair;
     P.o = reinterpret_cast<__nv_bfloat16*>(a.o);
     P.ld = (long long)kv_ld;
-    P.scale_log2 = (float)(1.4426950408889634 / sqrt(192.0));
+    P.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d));
     P.keys = a.keys;
     P.done = a.keys + (size_t)a.B * a.H;
-    P.sqrt_d = sqrtf(192.0f);
+    P.sqrt_d = sqrtf((float)d);
     P.accumulate = a.accumulate;
     P.s_max = a.s_max;
     P.s_bh = a.s_bh;
     P.status = device_status_ptr();
-    P.kst = kMlaKStages;
+    P.kst = mla_k_stages<NQK>();
     P.vst = kMlaVStages;
     static bool attr_set[64] = {false};
     int dev = current_device();
     if (dev < 0) return cudaErrorInvalidDevice;
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(attn_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+        cudaError_t e =
+            cudaFuncSetAttribute(attn_mla_kernel<NQK>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
     int grid = num_sms();
     if (grid > P.total_items) grid = P.total_items;
     P.band = std::max(1, std::min(a.B * a.H, (2 * grid + P.n_pair - 1) / P.n_pair));
-    TraceScope ts("attn_mla", stream);
-    return launch_pdl(attn_mla_kernel, dim3(grid), dim3(kAttnThreads), kAttnSmem, stream, P);
+    TraceScope ts(NQK == kMlaQkBlocks ? "attn_mla" : "attn", stream);
+    return launch_pdl(attn_mla_kernel<NQK>, dim3(grid), dim3(kAttnThreads), kAttnSmem, stream, P);
 }
 
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {
-    if (a.mla) return launch_attn_mla(a, stream);
+    if (a.mla) return launch_attn_tmem_p<kMlaQkBlocks>(a, stream);
+    if (a.dh == 128) return launch_attn_tmem_p<2>(a, stream);
     AttnParams P;
     memset(&P, 0, sizeof(P));
-    if (a.dh != 64 && a.dh != 128) return cudaErrorInvalidValue;
+    if (a.dh != 64) return cudaErrorInvalidValue;
     const uint64_t ld = (uint64_t)a.H * a.dh;
     if (!make_tmap_3d(&P.tmQ, a.q, ld, a.T, a.B, ld, ld * a.T, 64, kAttnBlk, 0)) return cudaErrorInvalidValue;
     if (!make_tmap_3d(&P.tmK, a.k, ld, a.T, a.B, ld, ld * a.T, 64, kAttnBlk, 0)) return cudaErrorInvalidValue;
@@ -1017,20 +990,15 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {
     P.s_max = a.s_max;
     P.s_bh = a.s_bh;
     P.status = device_status_ptr();
-    // after Q and P of two tiles: K and V rings of nc-block stages (4 + 4 at
-    // dh = 64; 2 + 1 at dh = 128, where V is needed a softmax later than K)
-    const int nc = a.dh / 64;
-    const int room = kAttnRing / kAttnTile - 2 * nc - 4;  // in 16 KB blocks
-    P.kst = nc == 1 ? 4 : 2;
-    P.vst = nc == 1 ? 4 : 1;
-    if ((P.kst + P.vst) * nc > room) return cudaErrorInvalidValue;
+    // after Q of two tiles: K and V rings of 4 + 4 one-block stages
+    P.kst = 4;
+    P.vst = 4;
+    static_assert((2 + 4 + 4) * kAttnTile <= kAttnRing, "attention shared memory");
     static bool attr_set[64] = {false};
     int dev = current_device();
     if (dev < 0) return cudaErrorInvalidDevice;
     if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+        cudaError_t e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
@@ -1038,8 +1006,7 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {
     if (grid > P.total_items) grid = P.total_items;
     P.band = std::max(1, std::min(a.B * a.H, (2 * grid + P.n_pair - 1) / P.n_pair));
     TraceScope ts("attn", stream);
-    return nc == 1 ? launch_pdl(attn_kernel<64>, dim3(grid), dim3(kAttnThreads), kAttnSmem, stream, P)
-                   : launch_pdl(attn_kernel<128>, dim3(grid), dim3(kAttnThreads), kAttnSmem, stream, P);
+    return launch_pdl(attn_kernel, dim3(grid), dim3(kAttnThreads), kAttnSmem, stream, P);
 }
 
 }  // namespace mc
