@@ -5,7 +5,8 @@ scan (a plugin inside a framework that owns every device allocation, or code
 running while its stream is captured into a CUDA graph): instead of a
 caller workspace it uses the library's own static device scratch.  Called
 here straight through the C ABI (ctypes) and through its Python wrapper,
-and checked against the workspace-taking entry point on the same inputs.
+and checked against the fp64 oracle and the workspace-taking entry point on
+the same inputs.
 Two calls in a row use different inputs, the second with logits 100 times
 smaller: the scratch keeps the first call's maximum keys, so the second
 result is only right if each call clears what must start at zero.
@@ -17,6 +18,7 @@ import pytest
 import torch
 
 import mc_inputs
+import oracle
 from gpu_helpers import SMAX_RTOL, dev, lib, rel_err
 
 pytestmark = pytest.mark.gpu
@@ -49,6 +51,9 @@ def test_noalloc_matches_workspace_entry_point():
             assert st == 0, api.mc_status_string(st)
             torch.cuda.synchronize()
             r = ref.cpu().numpy()
+            ref_o = oracle.max_logits_mha(inp["x"], wq_call.cpu(), inp["wk"], H, dh, causal)
+            assert rel_err(got_bh.cpu().numpy(), ref_o).max() < SMAX_RTOL
+            assert rel_err(got.cpu().numpy(), ref_o.max(0)).max() < SMAX_RTOL
             assert rel_err(got.cpu().numpy(), r).max() < SMAX_RTOL
             assert rel_err(got_bh.cpu().numpy(), ref_bh.cpu().numpy()).max() < SMAX_RTOL
             if prev is not None:
