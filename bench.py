@@ -79,11 +79,13 @@ def scan_pairs(B, T, causal):
 # expert-batch Newton-Schulz launch (cooperative, on CTA pairs) cannot be
 # captured by ncu and has no entry.  Drop an entry whenever the kernel changes.
 TRAFFIC = {
-    ("c2", "gemm:ns"): 4282112 + 22272,
+    ("c2", "gemm:ns"): 4287232 + 36608,
     ("c2", "scan"): 33612544,
     ("c3", "scan"): 2933748736 + 143360,
     ("c5", "scan"): 1450577664 + 3536896,
-    ("attn", "attn"): 50556416 + 814080,
+    ("attn", "attn"): 50554624 + 1516544,
+    ("attnl", "attn"): 208968192 + 49289216,
+    ("attn_mla", "attn_mla"): 2928908544 + 261668096,
 }
 
 
