@@ -903,6 +903,13 @@ bool ns_problem(GemmProblem& q, const NsPlan& P, const NsGroup& gr, int kind, in
     //   poly 0  fp16 A  -> bf16 B (B meets the bf16 X in the apply)
     //   apply 0 bf16 B, X -> fp16 X (scaled by s)
     // and every later GEMM reads and writes fp16.
+    // The apply X' = aX + BX reads X a second time, as the epilogue's aux.
+    // From the second iteration on, the poly adds a to its diagonal instead
+    // (B' = aI + B, the same product: X' = B'X), so the apply is a plain
+    // product whose epilogue reads nothing beside its accumulator.  Its
+    // entries round in fp16 once, at most 2^-10 on a diagonal below 4, less
+    // than X's own fp16 rounding.  The first apply keeps aX0 in fp32 from the
+    // unscaled bf16 X0, whose B is bf16 (a + B_ii would lose 2^-7 there).
     const int in_f16 = it == 0 ? (kind == 1) : 1;
     const int out_f16 = it == 0 ? (kind != 1) : 1;
     q.ab_f16 = in_f16;  // the aux operand (A in poly, X in apply) has the same type
@@ -938,6 +945,7 @@ bool ns_problem(GemmProblem& q, const NsPlan& P, const NsGroup& gr, int kind, in
         q.aux_bstride = mp * mp;
         q.alpha = c;
         q.beta = b;
+        if (it > 0) q.diag = a;  // B' = aI + bA + cA^2
     } else {
         if (!make_tmap_3d(&q.tmA, gr.Bm, mp, mp, cnt, mp, mp * mp, kBK, kBM, in_f16)) return false;
         if (!make_tmap_3d(&q.tmB, gr.X[xin], np, mp, cnt, np, mp * np, 64, stage_k_for(tile_m), in_f16))
@@ -949,12 +957,14 @@ bool ns_problem(GemmProblem& q, const NsPlan& P, const NsGroup& gr, int kind, in
         q.out = gr.X[xout];
         q.out_ld = np;
         q.out_bstride = mp * np;
-        q.aux = gr.X[xin];
-        q.aux_ld = np;
-        q.aux_bstride = mp * np;
         q.alpha = 1.f;
-        q.beta = a;
-        q.scale = it == 0 ? P.s + gr.zbase : nullptr;
+        if (it == 0) {  // X1 = s (a X0 + B X0)
+            q.aux = gr.X[xin];
+            q.aux_ld = np;
+            q.aux_bstride = mp * np;
+            q.beta = a;
+            q.scale = P.s + gr.zbase;
+        }  // later: X' = B' X
     }
     return true;
 }

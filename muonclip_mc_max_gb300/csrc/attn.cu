@@ -957,7 +957,12 @@ static cudaError_t launch_attn_tmem_p(const AttnArgs& a, cudaStream_t stream) {
     }
     int grid = num_sms();
     if (grid > P.total_items) grid = P.total_items;
-    P.band = std::max(1, std::min(a.B * a.H, (2 * grid + P.n_pair - 1) / P.n_pair));
+    // items per band: MLA half a round (its K and V, with a 16 KB row stride
+    // at K2's 64 heads, were re-read from DRAM three times over with two
+    // rounds: 2.35 vs 2.55 ms at [2, 8192, 64 heads]); MHA two rounds, whose
+    // heavy-first order balances the causal tail (0.61 vs 0.67 ms with one)
+    const int band_items = NQK == kMlaQkBlocks ? grid / 2 : 2 * grid;
+    P.band = std::max(1, std::min(a.B * a.H, (band_items + P.n_pair - 1) / P.n_pair));
     TraceScope ts(NQK == kMlaQkBlocks ? "attn_mla" : "attn", stream);
     return launch_pdl(attn_mla_kernel<NQK>, dim3(grid), dim3(kAttnThreads), kAttnSmem, stream, P);
 }

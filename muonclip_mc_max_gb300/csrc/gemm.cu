@@ -187,6 +187,17 @@ MC_D void store_f16x8(__half* dst, const float* v) {
     *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<uint4*>(h);
 }
 
+// The diagonal term: diag added to element (r, r) when the 32 x 64 chunk at
+// (row0, col0) meets the diagonal (a warp-uniform test); the column is
+// matched by an unrolled compare, so the values stay in registers.
+MC_D void add_diag(const GemmProblem& q, int row0, int col0, int r, float* f) {
+    if (q.diag == 0.f || col0 >= row0 + 32 || row0 >= col0 + 64) return;
+    const float dg = q.diag;
+#pragma unroll
+    for (int i = 0; i < 64; ++i)
+        if (col0 + i == r) f[i] = __fadd_rn(f[i], dg);
+}
+
 // Epilogue for 64 consecutive columns [col0, col0 + 64) of row r.
 MC_D void epilogue_chunk(const GemmProblem& q, int z, int r, int col0, float* f, float sc, unsigned* status) {
     if (r >= q.M || col0 >= q.N) return;
@@ -219,6 +230,7 @@ MC_D void epilogue_chunk(const GemmProblem& q, int z, int r, int col0, float* f,
 #pragma unroll
         for (int i = 0; i < 64; ++i) f[i] *= s;
     }
+    add_diag(q, r - (threadIdx.x & 31), col0, r, f);
     if (q.out_kind == kOutF16) {
         __half* o = reinterpret_cast<__half*>(q.out) + (size_t)z * q.out_bstride + (size_t)r * q.out_ld;
         bool big = false;
@@ -369,6 +381,7 @@ MC_D void chunk_values(const GemmProblem& q, int row0, int col0, float* f, float
             f[i + 1] = r.y;
         }
     }
+    add_diag(q, row0, col0, r, f);
 }
 
 // Warp-cooperative epilogue of a 32-row x 64-column chunk (rows row0.., one

@@ -41,7 +41,8 @@ constexpr int kPhaseProbs = 4;  // problems per phase (staged in shared memory)
 // One GEMM problem of a multi-problem launch: D[z] = A[z] * op(B[z]),
 // A [M][K] K-major; B K-major ([N][K]) or MN-major ([K][N]).
 // Operands are bf16 or (ab_f16) fp16.  Epilogue: v = scale[z] * (alpha *
-// acc + beta * aux[z][r][c]), optional RoPE on column chunks, then a bf16,
+// acc + beta * aux[z][r][c]) (+ diag where r == c), optional RoPE on column
+// chunks, then a bf16,
 // f32 or f16 store (f16 stores flag MC_DEV_RANGE when |v| > 65504); `sym`
 // stores only c >= r and mirrors it to (c, r) (M == N, only upper tiles are
 // scheduled).
@@ -65,7 +66,8 @@ struct GemmProblem {
     float alpha, beta;
     const float* scale;
     const float2* rope_tab;  // [rope_T][32] (cos, sin); null = no RoPE
-    int rope_T, rope_period, rope_start, pad_;
+    int rope_T, rope_period, rope_start;
+    float diag;  // added to the diagonal elements (row == column) of the output, after alpha, beta and the scale
 };
 
 // Per-matrix facts of a Muon batch, written to the workspace by the

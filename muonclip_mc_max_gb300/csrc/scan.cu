@@ -370,8 +370,10 @@ cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream) {
     }
     int grid = num_sms();
     if (grid > P.total_items) grid = P.total_items;
-    // about two rounds of items per band
-    P.band = std::max(1, std::min(a.B * a.H, (2 * grid + P.n_it - 1) / P.n_it));
+    // about one round of items per band: the band's K tiles then stay in L2
+    // (K2 MLA layer and the long-context scan 2.6-3.4% faster than with two
+    // rounds; the MHA layer the same)
+    P.band = std::max(1, std::min(a.B * a.H, (grid + P.n_it - 1) / P.n_it));
     P.stages = std::min(kScanMaxStages, (kScanRing - 2 * nkb * kQBlockBytes) / kKStageBytes);
     TraceScope ts("scan", stream);
     return launch_pdl(scan_kernel, dim3(grid), dim3(kScanThreads), kScanSmem, stream, P);
