@@ -79,13 +79,13 @@ def scan_pairs(B, T, causal):
 # expert-batch Newton-Schulz launch (cooperative, on CTA pairs) cannot be
 # captured by ncu and has no entry.  Drop an entry whenever the kernel changes.
 TRAFFIC = {
-    ("c2", "gemm:ns"): 4287232 + 36608,
-    ("c2", "scan"): 33612544,
-    ("c3", "scan"): 2933748736 + 143360,
-    ("c5", "scan"): 1450577664 + 3536896,
+    ("c2", "gemm:ns"): 4281600 + 3840,
+    ("c2", "scan"): 33608192 + 0,
+    ("c3", "scan"): 2765501696 + 3449344,
+    ("c5", "scan"): 1400462848 + 3004416,
     ("attn", "attn"): 50554624 + 1516544,
     ("attnl", "attn"): 208968192 + 49289216,
-    ("attn_mla", "attn_mla"): 2928908544 + 261668096,
+    ("attn_mla", "attn_mla"): 1360689920 + 252992768,
 }
 
 
