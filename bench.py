@@ -83,9 +83,9 @@ TRAFFIC = {
     ("c2", "scan"): 33608192 + 0,
     ("c3", "scan"): 2765501696 + 3449344,
     ("c5", "scan"): 1400462848 + 3004416,
-    ("attn", "attn"): 50554624 + 1516544,
-    ("attnl", "attn"): 208968192 + 49289216,
-    ("attn_mla", "attn_mla"): 1360689920 + 252992768,
+    ("attn", "attn"): 50564864 + 1067776,
+    ("attnl", "attn"): 536793600 + 47069696,
+    ("attn_mla", "attn_mla"): 1080236032 + 251761408,
 }
 
 

@@ -907,6 +907,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_mla_kernel(const __grid_
     }
 }
 
+// Items per band of the MHA forward: eight rounds.  With few (sequence,
+// head) pairs the causal tail is the limit, and the heavy-first order within
+// a band only balances it when the band spans many rounds: [2, 8192, 16
+// heads] causal ran 0.485 ms at dh = 128 and 0.414 ms at dh = 64 with one
+// band of all 32 pairs, against 0.609 and 0.525 ms with two rounds per band.
+static int attn_band_items(int grid) { return 8 * grid; }
+
 // The P-in-TMEM kernel: MLA (d = 192 over q^C, k^C and the shared k^R) or,
 // with NQK = 2, MHA at dh = 128.
 template <int NQK>
@@ -957,11 +964,11 @@ static cudaError_t launch_attn_tmem_p(const AttnArgs& a, cudaStream_t stream) {
     }
     int grid = num_sms();
     if (grid > P.total_items) grid = P.total_items;
-    // items per band: MLA half a round (its K and V, with a 16 KB row stride
-    // at K2's 64 heads, were re-read from DRAM three times over with two
-    // rounds: 2.35 vs 2.55 ms at [2, 8192, 64 heads]); MHA two rounds, whose
-    // heavy-first order balances the causal tail (0.61 vs 0.67 ms with one)
-    const int band_items = NQK == kMlaQkBlocks ? grid / 2 : 2 * grid;
+    // items per band: MLA a quarter of a round (its K and V, with a 16 KB
+    // row stride at K2's 64 heads, were re-read from DRAM three times over
+    // with two rounds: 2.28 ms with a quarter, 2.35 with a half, 2.55 with two
+    // at [2, 8192, 64 heads]); MHA eight rounds (attn_band_items)
+    const int band_items = NQK == kMlaQkBlocks ? grid / 4 : attn_band_items(grid);
     P.band = std::max(1, std::min(a.B * a.H, (band_items + P.n_pair - 1) / P.n_pair));
     TraceScope ts(NQK == kMlaQkBlocks ? "attn_mla" : "attn", stream);
     return launch_pdl(attn_mla_kernel<NQK>, dim3(grid), dim3(kAttnThreads), kAttnSmem, stream, P);
@@ -1009,7 +1016,7 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {
     }
     int grid = num_sms();
     if (grid > P.total_items) grid = P.total_items;
-    P.band = std::max(1, std::min(a.B * a.H, (2 * grid + P.n_pair - 1) / P.n_pair));
+    P.band = std::max(1, std::min(a.B * a.H, (attn_band_items(grid) + P.n_pair - 1) / P.n_pair));
     TraceScope ts("attn", stream);
     return launch_pdl(attn_kernel, dim3(grid), dim3(kAttnThreads), kAttnSmem, stream, P);
 }
