@@ -916,7 +916,10 @@ bool ns_problem(GemmProblem& q, const NsPlan& P, const NsGroup& gr, int kind, in
     q.out_kind = out_f16 ? kOutF16 : kOutBF16;
     // workspace buffers: 256-byte aligned, rows of m_pad / n_pad (multiples of 64) elements
     q.bulk_st = kind == 2 || !sym;
-    if (q.bulk_st) {
+    // symmetric Gram and poly outputs: their chunks above the diagonal go out
+    // by TMA stores too, the rows and (transposed by a pair of warps) the mirror
+    q.sym_tma = sym && kind != 2;
+    if (q.bulk_st || q.sym_tma) {
         const void* out = kind == 0 ? (const void*)gr.A : kind == 1 ? (const void*)gr.Bm : (const void*)gr.X[xout];
         const uint64_t on = kind == 2 ? np : mp;
         if (!make_tmap_3d(&q.tmC, out, on, mp, cnt, on, mp * on, 64, 32, out_f16)) return false;

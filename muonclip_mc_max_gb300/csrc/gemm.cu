@@ -76,6 +76,7 @@ struct GemmSmemTail {
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
+    uint64_t pairbar[2];  // the epilogue's two pairs of warps (rows 0-63 and 64-127 of a CTA's tile)
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -151,7 +152,7 @@ MC_D void grid_sync(const GemmParamsT<MAXP>& P, int seq, volatile int* abort_fla
             for (int i = P.phase_prob[next_ph]; i < P.phase_prob[next_ph + 1]; ++i) {
                 tma_prefetch_desc(&P.p[i].tmA);
                 tma_prefetch_desc(&P.p[i].tmB);
-                if (P.p[i].bulk_st) tma_prefetch_desc(&P.p[i].tmC);
+                if (P.p[i].bulk_st || P.p[i].sym_tma) tma_prefetch_desc(&P.p[i].tmC);
             }
         const unsigned target = (unsigned)(seq + 1) * gridDim.x;
         uint64_t t0 = 0;
@@ -471,6 +472,94 @@ MC_D void epilogue_chunk_staged(const GemmProblem& q, int z, int row0, int col0,
     }
 }
 
+// The two warps whose rows form one 64-row half of the tile meet here:
+// lane 0 of each arrives, every lane waits (bounded).  false (in every
+// lane) when the wait gave up.
+MC_D bool pair_sync(uint64_t* bar, uint32_t& ph, volatile int* abort_flag, unsigned* status) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+    const bool ok = mbar_wait(bar, ph, abort_flag, status);
+    ph ^= 1;
+    return ok;
+}
+
+// Symmetric 16-bit output, a 32 x 64 chunk wholly above the diagonal of its
+// pair of warps (every column right of the pair's 64 rows): the rows go out
+// as one TMA tensor store of the chunk, and the mirrored rows as two more.
+// The pair transposes its 64 x 64 region into two {64, 32} boxes, rows
+// c0 .. c0 + 31 in the buffer of the warp with the lower rows (S when low)
+// and rows c0 + 32 .. c0 + 63 in the other's (Sp), each warp writing its 32
+// columns of both; each warp then stores the box in its own buffer.  Four
+// epilogue warps issue one global request per 128-byte row segment at about
+// one per 15 cycles per SM; three TMA stores replace the 512 requests of the
+// coalesced row and mirror stores.  The values are rounded once: the mirror
+// holds the same 16-bit values as the rows.
+MC_D bool epilogue_chunk_sym_tma(const GemmProblem& q, int z, int row0, int col0, float* f, float sc,
+                                 uint16_t* S, uint64_t* pairbar, uint32_t& pph, unsigned* status, uint4 (&u)[8],
+                                 int next_col0, const CUtensorMap* tmC, volatile int* abort_flag) {
+    const int lane = threadIdx.x & 31;
+    // warps 2 / 3 and 4 / 5 pair up (rows 64-127 and 0-63 of the tile); the
+    // even warp holds the lower 32 rows, and the buffers are adjacent
+    const int warp = threadIdx.x >> 5;
+    const bool low = (warp & 1) == 0;
+    uint16_t* Sp = S + (low ? 1 : -1) * (kEpiWarpBytes / 2);
+    uint64_t* pbar = pairbar + ((warp & 3) >> 1);
+    bulk_wait_read();  // this warp's stores of the previous chunk have read S
+    __syncwarp();
+    chunk_values(q, row0, col0, f, sc, S, u, true);
+    if (q.aux && next_col0 >= 0 && next_col0 < q.N) aux_load(q, z, row0, next_col0, u);
+    const bool f16 = q.out_kind == kOutF16;
+    if (f16) {
+        float mx = 0.f;
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) mx = fmaxf(mx, fmaxf(fabsf(f[i]), fabsf(f[i + 1])));
+        if (mx > 65504.0f) set_status(status, MC_DEV_RANGE);
+    }
+    // the 16-bit values, rounded once for the rows and the mirror
+    uint4 pk[8];
+#pragma unroll
+    for (int v = 0; v < 8; ++v) pk[v] = pack8(f + 8 * v, f16);
+    // both warps are past their aux staging in S and their previous stores
+    // out of it: each warp's buffer is free for its own rows
+    if (!pair_sync(pbar, pph, abort_flag, status)) return false;
+#pragma unroll
+    for (int v = 0; v < 8; ++v) *reinterpret_cast<uint4*>(S + stage_off(true, lane, v)) = pk[v];
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_3d(tmC, S, col0, row0, z);
+        bulk_commit();
+    }
+    bulk_wait_read();  // the rows have been read out of S
+    __syncwarp();
+    // both buffers are free: the transposed halves go into both
+    if (!pair_sync(pbar, pph, abort_flag, status)) return false;
+    const int e = lane + (low ? 0 : 32);  // this row's column in the transposed boxes
+    const int seg = e >> 3, el = e & 7;
+    uint16_t* bA = low ? S : Sp;  // transposed rows c0 .. c0 + 31
+    uint16_t* bB = low ? Sp : S;  // transposed rows c0 + 32 .. c0 + 63
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+        uint16_t* b = v < 4 ? bA : bB;
+        const uint32_t w[4] = {pk[v].x, pk[v].y, pk[v].z, pk[v].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int i = (v & 3) * 8 + 2 * k;  // row of the transposed box
+            b[stage_off(true, i, seg) + el] = (uint16_t)(w[k] & 0xFFFFu);
+            b[stage_off(true, i + 1, seg) + el] = (uint16_t)(w[k] >> 16);
+        }
+    }
+    fence_proxy_async_smem();
+    // the other warp's half of this warp's box is written and fenced
+    if (!pair_sync(pbar, pph, abort_flag, status)) return false;
+    if (lane == 0) {
+        tma_store_3d(tmC, S, row0 - (low ? 0 : 32), col0 + (low ? 0 : 32), z);
+        bulk_commit();
+    }
+    __syncwarp();
+    return true;
+}
+
 // Pre-phase of a multi-phase Newton-Schulz launch: s = 1 / (||U||_F + eps)
 // and s^2 from the momentum pass's per-tile sums of squares, one matrix per
 // CTA at a time, summed in a fixed order.
@@ -530,6 +619,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             mbar_init(&tail->tempty[a], PAIR ? 8 : 4);  // pair: both CTAs' epilogue warps
         }
         mbar_init(&tail->drain, 1);
+        for (int pr = 0; pr < 2; ++pr) mbar_init(&tail->pairbar[pr], 2);  // lane 0 of both warps
         tail->abort_flag = 0;
         fence_mbar_init();
     }
@@ -537,7 +627,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         for (int i = 0; i < P.nprob; ++i) {
             tma_prefetch_desc(&P.p[i].tmA);
             tma_prefetch_desc(&P.p[i].tmB);
-            if (P.p[i].bulk_st) tma_prefetch_desc(&P.p[i].tmC);
+            if (P.p[i].bulk_st || P.p[i].sym_tma) tma_prefetch_desc(&P.p[i].tmC);
         }
     }
     if (warp == 1) {
@@ -560,6 +650,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     // role state, carried across phases
     int stage = 0, acc = 0;
     uint32_t phase = 0, aphase = 0;
+    uint32_t pph = 0;  // epilogue warps: phase of their pair's barrier
     uint32_t issued[STAGES];
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) issued[s] = 0;
@@ -737,7 +828,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                     tmem_ld32(taddr, v);
                     tmem_ld32(taddr + 32, v + 32);
                     tmem_ld_wait();
-                    if (staged)
+                    const int col0 = tn * BN + c * 64;
+                    const int pair_row0 = row0 & ~63;  // the pair's 64 rows (row blocks are multiples of 64)
+                    // CTA-pair tiles only: the single-CTA launches of small
+                    // batches keep the compact epilogue
+                    if (PAIR && staged && q.sym_tma && col0 >= pair_row0 + 64 && pair_row0 + 64 <= q.M &&
+                        col0 + 64 <= q.N) {
+                        if (!epilogue_chunk_sym_tma(q, z, row0, col0, reinterpret_cast<float*>(v), sc, S,
+                                                    tail->pairbar, pph, P.status, u,
+                                                    c + 1 < BN / 64 ? tn * BN + (c + 1) * 64 : -1,
+                                                    &P.p[pb + pi].tmC, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                    } else if (staged)
                         epilogue_chunk_staged(q, z, row0, tn * BN + c * 64, reinterpret_cast<float*>(v), sc, S,
                                               P.status, u, c + 1 < BN / 64 ? tn * BN + (c + 1) * 64 : -1,
                                               &P.p[pb + pi].tmC);

@@ -68,7 +68,10 @@ struct GemmProblem {
     const float2* rope_tab;  // [rope_T][32] (cos, sin); null = no RoPE
     int rope_T, rope_period, rope_start;
     float diag;  // added to the diagonal elements (row == column) of the output, after alpha, beta and the scale
+    int sym_tma;  // sym with a 16-bit output and tmC: chunks above the diagonal go out by TMA stores (rows and mirror)
+    int pad_[3];
 };
+static_assert(sizeof(GemmProblem) % 16 == 0, "problems are staged in 16-byte pieces");
 
 // Per-matrix facts of a Muon batch, written to the workspace by the
 // momentum pass and read by the norm pre-phase of the multi-phase
