@@ -8,8 +8,9 @@ properties that hold at any size cover the rest.
               and the clip bit-exact, both Muon matrices.
   K2 MLA      x [16,4096,7168] causal: every head of two sequences and one
               rotating head of each of the other 14.
-  expert batch 96 matrices of 7168x2048 / 2048x7168: two matrices against
-              the oracle, every matrix's momentum and update RMS checked.
+  expert batch 96 matrices of 7168x2048 / 2048x7168: eight matrices (four
+              tall, four wide) against the oracle, every matrix's update
+              RMS checked.
   long MLA    x [1,32768,7168] causal + heavy rows: the 8 planted heads and
               8 cold ones, the MLA clip bit-exact, Muon on W_kva and W_kb
               against the oracle.
@@ -117,7 +118,9 @@ def test_expert_batch_fullsize():
     lib()
     from muonclip_mc_max_gb300 import api
     inp = mc_inputs.c4(device=dev())
-    picks = [0, 95]  # one tall (7168 x 2048), one wide (2048 x 7168)
+    # four tall (7168 x 2048) and four wide (2048 x 7168) matrices, spread
+    # over the batch and so over the tiles and phases of the launch
+    picks = [0, 17, 31, 47, 48, 63, 80, 95]
     w0 = {i: inp["w"][i].cpu() for i in picks}
     m0 = {i: inp["m_prev"][i].cpu() for i in picks + [1, 50]}
     wcopy = [t.clone() for t in inp["w"]]
