@@ -51,6 +51,9 @@ def _check(q, k, v, H, dh, causal):
     (1, 128, 1, 64),    # exactly one tile
     (2, 77, 2, 64),     # T below one tile
     (1, 1030, 1, 64),   # nine key blocks, tail of 6
+    (2, 77, 2, 128),    # dh = 128 below one tile
+    (2, 200, 2, 128),   # dh = 128, two query tiles, ragged key tail
+    (1, 1030, 1, 128),  # dh = 128, nine key blocks through its two K stages
 ])
 def test_attention_vs_oracle(shape, causal):
     B, T, H, dh = shape
