@@ -90,6 +90,11 @@ size_t mc_max_logits_mha_workspace_size(int B, int T, int D, int H, int dh, mc_d
  *   s_max    [H] f32 out.  accumulate != 0 max-merges into the existing
  *            values (max over micro-batches); NaN propagates.
  *   s_max_bh [B][H] f32 out (per-sequence maxima), may be NULL.
+ *            On the tensor-core path the scan kernel merges each work
+ *            item's maximum into s_max / s_max_bh with integer atomics
+ *            (the call first fills them with 0xFFFFFFFF, s_max only when
+ *            not accumulating); both hold the result once the stream has
+ *            passed the call.
  *   ws       workspace of ws_bytes >= mc_max_logits_mha_workspace_size,
  *            256-byte aligned.
  * bf16 with D % 8 == 0 and dh in {64, 128, 192} runs on tcgen05 tensor
@@ -191,8 +196,9 @@ mc_status mc_max_logits_mla(const mc_mla_layer* layer, const void* x, int B, int
  * dh must be 64 or 128; pointers 16-byte aligned; T >= 1.  Tensor cores
  * compute q.k and P.v with fp32 accumulation; the softmax weights P are
  * rounded once to bf16 for P.v.  NaN logits make s_max NaN and set
- * MC_DEV_NONFINITE.  ws: at least mc_attention_mha_workspace_size(B, H)
- * bytes, 256-byte aligned.
+ * MC_DEV_NONFINITE.  s_max / s_max_bh are merged into by the forward kernel
+ * as for the scan.  No workspace is needed: mc_attention_mha_workspace_size
+ * returns 0 and ws / ws_bytes are ignored (NULL and 0 are fine).
  */
 size_t mc_attention_mha_workspace_size(int B, int H);
 mc_status mc_attention_mha(const void* q, const void* k, const void* v, int B, int T, int H, int dh,
@@ -215,8 +221,7 @@ mc_status mc_attention_mha(const void* q, const void* k, const void* v, int B, i
  * Supported: nope = 128, rope = 64, dv = 128 (K2's MLA; else
  * MC_ERR_UNSUPPORTED).  kr_ld and kr_col multiples of 8; pointers 16-byte
  * aligned; o must not alias an input.  Precision, NaN handling, s_max_bh,
- * accumulate and the workspace (mc_attention_mha_workspace_size(B, H)) as
- * for mc_attention_mha.
+ * accumulate and the (unused) workspace as for mc_attention_mha.
  */
 mc_status mc_attention_mla(const void* q, const void* k_c, const void* k_r, int kr_ld, int kr_col,
                            const void* v, int B, int T, int H, int nope, int rope, int dv,

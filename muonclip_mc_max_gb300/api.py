@@ -178,6 +178,8 @@ _default_ws: dict = {}
 
 
 def _ws(workspace, nbytes, device):
+    if nbytes == 0:
+        return ctypes.c_void_p(None), 0
     if workspace is None:
         workspace = _default_ws.setdefault(str(device), Workspace())
     buf = workspace.get(nbytes, device)

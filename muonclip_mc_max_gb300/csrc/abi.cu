@@ -343,23 +343,37 @@ int mc_trace_collect(mc_trace_entry* out, int cap, int keep) {
 
 static bool mha_tensor_path(mc_dtype dt, int D, int dh) { return dt == MC_BF16 && D % 8 == 0 && dh % 64 == 0 && dh <= 192; }
 
+// The tensor-core scans and attention forwards max-merge S straight into the
+// caller's s_max / s_bh with integer atomics (no pass after the kernel):
+// every word starts at 0xFFFFFFFF, which sorts below every value, except
+// that s_max keeps its maxima when the call accumulates.
+static cudaError_t reset_smax(float* s_max, float* s_bh, int B, int H, int accumulate, cudaStream_t stream) {
+    if (!accumulate) {
+        cudaError_t e = cudaMemsetAsync(s_max, 0xFF, sizeof(float) * (size_t)H, stream);
+        if (e != cudaSuccess) return e;
+    }
+    return s_bh ? cudaMemsetAsync(s_bh, 0xFF, sizeof(float) * (size_t)B * H, stream) : cudaSuccess;
+}
+
 static size_t mha_carve(Carve& c, int B, int T, int D, int H, int dh, mc_dtype dt, void** q, void** k,
                         unsigned** keys) {
     const size_t n = mul_sat((size_t)B * T, (size_t)H * dh);
     if (mha_tensor_path(dt, D, dh)) {
         *q = c.take<__half>(n);
         *k = c.take<__half>(n);
+        *keys = nullptr;
     } else {
         *q = c.take<float>(n);
         *k = c.take<float>(n);
+        *keys = c.take<unsigned>((size_t)B * H);  // the CUDA-core scan's per-(b, h) keys
     }
-    *keys = c.take<unsigned>((size_t)B * H + 1);  // + the scan's done-counter
     return c.used;
 }
 
 size_t mc_attention_mha_workspace_size(int B, int H) {
-    if (B <= 0 || H <= 0) return 0;
-    return align256(sizeof(unsigned) * ((size_t)B * H + 1));
+    (void)B;
+    (void)H;
+    return 0;  // the forwards merge S_max straight into the outputs
 }
 
 mc_status mc_attention_mha(const void* q, const void* k, const void* v, int B, int T, int H, int dh, int causal,
@@ -372,10 +386,9 @@ mc_status mc_attention_mha(const void* q, const void* k, const void* v, int B, i
     if ((int64_t)B * T > INT32_MAX || (int64_t)H * dh > INT32_MAX) return MC_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return MC_ERR_INVALID_ARG;
     if (o == q || o == k || o == v) return MC_ERR_INVALID_ARG;
-    const size_t need = mc_attention_mha_workspace_size(B, H);
-    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < need) return MC_ERR_WORKSPACE;
-    unsigned* keys = (unsigned*)ws;
-    MC_CUDA(cudaMemsetAsync(keys, 0, sizeof(unsigned) * ((size_t)B * H + 1), stream));
+    (void)ws;  // no workspace: S_max is merged straight into s_max / s_max_bh
+    (void)ws_bytes;
+    MC_CUDA(reset_smax(s_max, s_max_bh, B, H, accumulate, stream));
     AttnArgs a;
     memset(&a, 0, sizeof(a));
     a.q = q;
@@ -387,8 +400,6 @@ mc_status mc_attention_mha(const void* q, const void* k, const void* v, int B, i
     a.H = H;
     a.dh = dh;
     a.causal = causal ? 1 : 0;
-    a.keys = keys;
-    a.accumulate = accumulate ? 1 : 0;
     a.s_max = s_max;
     a.s_bh = s_max_bh;
     MC_CUDA(launch_attn(a, stream));
@@ -406,10 +417,9 @@ mc_status mc_attention_mla(const void* q, const void* k_c, const void* k_r, int 
     if (kr_col < 0 || kr_ld < kr_col + rope || kr_ld % 8 || kr_col % 8) return MC_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_c) || !aligned16(k_r) || !aligned16(v) || !aligned16(o)) return MC_ERR_INVALID_ARG;
     if (o == q || o == k_c || o == k_r || o == v) return MC_ERR_INVALID_ARG;
-    const size_t need = mc_attention_mha_workspace_size(B, H);
-    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < need) return MC_ERR_WORKSPACE;
-    unsigned* keys = (unsigned*)ws;
-    MC_CUDA(cudaMemsetAsync(keys, 0, sizeof(unsigned) * ((size_t)B * H + 1), stream));
+    (void)ws;  // no workspace: S_max is merged straight into s_max / s_max_bh
+    (void)ws_bytes;
+    MC_CUDA(reset_smax(s_max, s_max_bh, B, H, accumulate, stream));
     AttnArgs a;
     memset(&a, 0, sizeof(a));
     a.q = q;
@@ -425,8 +435,6 @@ mc_status mc_attention_mla(const void* q, const void* k_c, const void* k_r, int 
     a.H = H;
     a.dh = nope + rope;
     a.causal = causal ? 1 : 0;
-    a.keys = keys;
-    a.accumulate = accumulate ? 1 : 0;
     a.s_max = s_max;
     a.s_bh = s_max_bh;
     MC_CUDA(launch_attn(a, stream));
@@ -455,9 +463,9 @@ mc_status mc_max_logits_mha(const void* x, const void* wq, const void* wk, mc_dt
     void *q, *k;
     unsigned* keys;
     mha_carve(c, B, T, D, H, dh, dtype, &q, &k, &keys);
-    MC_CUDA(cudaMemsetAsync(keys, 0, sizeof(unsigned) * ((size_t)B * H + 1), stream));
     const int64_t BT = (int64_t)B * T, N = (int64_t)H * dh;
     if (mha_tensor_path(dtype, D, dh)) {
+        MC_CUDA(reset_smax(s_max, s_max_bh, B, H, accumulate, stream));
         if (!aligned16(x) || !aligned16(wq) || !aligned16(wk)) return MC_ERR_INVALID_ARG;
         GemmParams P;
         memset(&P, 0, sizeof(P));
@@ -482,13 +490,12 @@ mc_status mc_max_logits_mha(const void* x, const void* wq, const void* wk, mc_dt
         a.k_head_stride = dh;
         a.nkb_main = dh / 64;
         a.nkb_rope = 0;
-        a.keys = keys;
         a.d = (float)dh;
-        a.accumulate = accumulate;
         a.s_max = s_max;
         a.s_bh = s_max_bh;
-        MC_CUDA(launch_scan(a, stream));  // finalises S_max in its last CTA
+        MC_CUDA(launch_scan(a, stream));  // merges S into s_max / s_max_bh
     } else {
+        MC_CUDA(cudaMemsetAsync(keys, 0, sizeof(unsigned) * (size_t)B * H, stream));
         MC_CUDA(launch_proj_simt(x, wq, dtype, (float*)q, (int)BT, D, (int)N, stream));
         MC_CUDA(launch_proj_simt(x, wk, dtype, (float*)k, (int)BT, D, (int)N, stream));
         MC_CUDA(launch_scan_simt((const float*)q, (const float*)k, B, T, H, dh, causal ? 1 : 0, keys, stream));
@@ -549,7 +556,6 @@ static mc_status mla_check(const mc_mla_layer* L, bool scan) {
 struct MlaWs {
     float2* rope;
     __half *cq, *ckv, *q, *kc, *wqb, *wkb;  // fp16 intermediates and fp16 copies of W_qb, W_kb
-    unsigned* keys;
 };
 
 static size_t mla_carve(Carve& c, const mc_mla_layer* L, int B, int T, MlaWs& w) {
@@ -562,7 +568,6 @@ static size_t mla_carve(Carve& c, const mc_mla_layer* L, int B, int T, MlaWs& w)
     w.kc = c.take<__half>(mul_sat(BT, H, L->nope));
     w.wqb = c.take<__half>(mul_sat(L->q_lora, H, qk));
     w.wkb = c.take<__half>(mul_sat(L->kv_lora, H, L->nope));
-    w.keys = c.take<unsigned>((size_t)B * H + 1);  // + the scan's done-counter
     return c.used;
 }
 
@@ -589,7 +594,7 @@ mc_status mc_max_logits_mla(const mc_mla_layer* L, const void* x, int B, int T, 
     mla_carve(c, L, B, T, w);
     const int64_t BT = (int64_t)B * T;
     const int qk = L->nope + L->rope, kvw = L->kv_lora + L->rope;
-    MC_CUDA(cudaMemsetAsync(w.keys, 0, sizeof(unsigned) * ((size_t)B * L->H + 1), stream));
+    MC_CUDA(reset_smax(s_max, s_max_bh, B, L->H, accumulate, stream));
     MC_CUDA(launch_rope_table(w.rope, T, L->rope_base, stream));
     // phase 1: c_Q = x W_qa ; [c_KV | k^R] = x W_kva (RoPE on the k^R columns)
     GemmParams P;
@@ -642,12 +647,10 @@ mc_status mc_max_logits_mla(const mc_mla_layer* L, const void* x, int B, int T, 
     a.nkb_main = L->nope / 64;
     a.nkb_rope = 1;
     a.kr_col = L->kv_lora;
-    a.keys = w.keys;
     a.d = (float)qk;
-    a.accumulate = accumulate;
     a.s_max = s_max;
     a.s_bh = s_max_bh;
-    MC_CUDA(launch_scan(a, stream));  // finalises S_max in its last CTA
+    MC_CUDA(launch_scan(a, stream));  // merges S into s_max / s_max_bh
     return MC_OK;
 }
 

@@ -20,9 +20,9 @@
 //   warpgroups 1, 2   one query row per thread of tile 0 / tile 1: S_t from
 //               TMEM, the raw row max (for S_max), the running softmax max m
 //               and sum l, O_t rescaled in TMEM when m moves, P_t = 2^(s - m)
-//               as bf16; at the end of the item O_t / l as bf16 and one
-//               atomicMax per warp on the monotonic key of (b, h)
-// The last CTA turns the keys into S_max (key / sqrt(dh)), like the scan.
+//               as bf16; at the end of the item O_t / l as bf16, and per
+//               warp S = max / sqrt(dh) max-merged into S_max[h] (and
+//               S_max[b, h]) by one integer atomic each, as in the scan
 #include "common.cuh"
 #include "internal.h"
 
@@ -57,10 +57,7 @@ struct AttnParams {
     __nv_bfloat16* o;
     long long ld;               // H * dh: row stride of q, k, v and o
     float scale_log2;           // log2(e) / sqrt(dh)
-    unsigned* keys;             // [B*H] monotonic keys of the raw max, then a done counter
-    unsigned* done;
     float sqrt_d;
-    int accumulate;
     float* s_max;
     float* s_bh;
     unsigned* status;
@@ -77,7 +74,6 @@ struct AttnSmemTail {
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
-    int last_cta;
 };
 
 // 2^x with the hardware approximation (relative error about 2^-22, far below
@@ -482,7 +478,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
             if (lane == 0) mbar_arrive(&tail->oempty[t]);
             // S_max: the raw max of the rows inside the sequence
             const float mw = warp_max_nan(row_ok ? m_raw : -INFINITY);
-            if (lane == 0 && mw != -INFINITY) atomicMax(&P.keys[b * P.H + h], float_key(mw));
+            if (lane == 0 && mw != -INFINITY)  // -inf: every row of this warp is past T
+                merge_smax(mw, P.sqrt_d, P.s_max, P.s_bh, b, P.H, h, P.status);
         }
     }
 
@@ -491,18 +488,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, 512);
-    // the last CTA to finish turns the keys into S_max
-    if (threadIdx.x == 0) {
-        __threadfence();
-        const unsigned old = atomicAdd(P.done, 1u);
-        tail->last_cta = old == gridDim.x - 1;
-    }
-    __syncthreads();
-    if (tail->last_cta) {
-        __threadfence();
-        for (int h = threadIdx.x; h < P.H; h += blockDim.x)
-            finalize_head(P.keys, P.B, P.H, h, P.sqrt_d, P.accumulate, P.s_max, P.s_bh, P.status);
-    }
 }
 
 // ---------------------------------------------------------------------------
@@ -885,7 +870,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_mla_kernel(const __grid_
             __syncwarp();
             if (lane == 0) mbar_arrive(&tail->oempty[t]);
             const float mw = warp_max_nan(row_ok ? m_raw : -INFINITY);
-            if (lane == 0 && mw != -INFINITY) atomicMax(&P.keys[b * P.H + h], float_key(mw));
+            if (lane == 0 && mw != -INFINITY)  // -inf: every row of this warp is past T
+                merge_smax(mw, P.sqrt_d, P.s_max, P.s_bh, b, P.H, h, P.status);
         }
     }
 
@@ -894,17 +880,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_mla_kernel(const __grid_
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, 512);
-    if (threadIdx.x == 0) {
-        __threadfence();
-        const unsigned old = atomicAdd(P.done, 1u);
-        tail->last_cta = old == gridDim.x - 1;
-    }
-    __syncthreads();
-    if (tail->last_cta) {
-        __threadfence();
-        for (int h = threadIdx.x; h < P.H; h += blockDim.x)
-            finalize_head(P.keys, P.B, P.H, h, P.sqrt_d, P.accumulate, P.s_max, P.s_bh, P.status);
-    }
 }
 
 // Items per band of the MHA forward: eight rounds.  With few (sequence,
@@ -944,10 +919,7 @@ static cudaError_t launch_attn_tmem_p(const AttnArgs& a, cudaStream_t stream) {
     P.o = reinterpret_cast<__nv_bfloat16*>(a.o);
     P.ld = (long long)kv_ld;
     P.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d));
-    P.keys = a.keys;
-    P.done = a.keys + (size_t)a.B * a.H;
     P.sqrt_d = sqrtf((float)d);
-    P.accumulate = a.accumulate;
     P.s_max = a.s_max;
     P.s_bh = a.s_bh;
     P.status = device_status_ptr();
@@ -995,10 +967,7 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {
     P.o = reinterpret_cast<__nv_bfloat16*>(a.o);
     P.ld = (long long)ld;
     P.scale_log2 = (float)(1.4426950408889634 / sqrt((double)a.dh));
-    P.keys = a.keys;
-    P.done = a.keys + (size_t)a.B * a.H;
     P.sqrt_d = sqrtf((float)a.dh);
-    P.accumulate = a.accumulate;
     P.s_max = a.s_max;
     P.s_bh = a.s_bh;
     P.status = device_status_ptr();

@@ -326,6 +326,29 @@ MC_D float warp_max_nan(float v) {
     return v;
 }
 
+// Max-merge of v into *addr in the float order with NaN above +inf: values
+// with the sign bit clear compare as signed integers, values with it set as
+// reversed unsigned integers, so one integer atomic merges each value.
+// *addr holds a float or the pattern 0xFFFFFFFF, which sorts below every
+// value; NaN is merged as the canonical positive NaN.
+MC_D void atomic_max_float(float* addr, float v) {
+    uint32_t u = __float_as_uint(v);
+    if (isnan(v)) u = 0x7FFFFFFFu;
+    if (u & 0x80000000u) atomicMin(reinterpret_cast<unsigned*>(addr), u);
+    else atomicMax(reinterpret_cast<int*>(addr), (int)u);
+}
+
+// A work item's raw maximum m merged into S_max[h], and into S_max[b, h]
+// when s_bh is given, as S = m / sqrt(d): the division is monotonic, so the
+// merged value is the maximum logit over the items divided once.  A
+// non-finite S sets the status bit.
+MC_D void merge_smax(float m, float sqrt_d, float* s_max, float* s_bh, int b, int H, int h, unsigned* status) {
+    const float s = __fdiv_rn(m, sqrt_d);
+    if (!isfinite(s)) set_status(status, MC_DEV_NONFINITE);
+    atomic_max_float(s_max + h, s);
+    if (s_bh) atomic_max_float(s_bh + (size_t)b * H + h, s);
+}
+
 // S_max[h] = max over sequences of key / sqrt(d) (NaN propagates); the
 // per-sequence maxima are written too when s_bh is given.
 MC_D void finalize_head(const unsigned* keys, int B, int H, int h, float sqrt_d, int accumulate,

@@ -158,10 +158,10 @@ struct ScanArgs {
     int nkb_main;        // 64-wide K blocks per head read from K main
     int nkb_rope;        // 0 or 1 block read from k^R at column kr_col
     int kr_col;
-    unsigned* keys;      // [B*H] monotonic keys (max-merged), then a zeroed done-counter
-    // finalisation, done by the last CTA to finish: S = key / sqrt(d)
     float d;
-    int accumulate;
+    // S = max / sqrt(d) is max-merged into s_max[H] (and s_bh[B][H] when
+    // given), which hold 0xFFFFFFFF in every word before the launch, or the
+    // maxima the scan accumulates into
     float* s_max;
     float* s_bh;
 };
@@ -177,8 +177,7 @@ struct AttnArgs {
     int mla;             // 1: MLA with nope = 128, rope = 64, dv = 128 (dh = 192 for the logits)
     void* o;             // bf16 [B][T][H*dh]; MLA: [B][T][H*dv]
     int B, T, H, dh, causal;
-    unsigned* keys;      // [B*H] zeroed monotonic keys, then a zeroed done counter
-    int accumulate;
+    // S = max / sqrt(dh) merged into s_max / s_bh as in the scan
     float* s_max;
     float* s_bh;
 };

@@ -16,8 +16,9 @@
 //   warp 1      tcgen05.mma Q K^T into one of two 128 x 256 fp32 TMEM tiles
 //   warps 2..5  tcgen05.ld -> running row max (max.NaN, 4 chains) with the
 //               causal / sequence-end mask only on edge tiles; at the end of
-//               the item a warp max and one atomicMax per warp on the
-//               monotonic key of (b, h)
+//               the item a warp max, and per warp S = max / sqrt(d)
+//               max-merged into S_max[h] (and S_max[b, h]) by one integer
+//               atomic each: the outputs need no pass after the scan
 // MLA items accumulate d = nope + rope = 192 as three K blocks: two q^C.k^C
 // blocks from the per-head k^C storage and one q^R.k^R block from the
 // shared k^R storage, all into the same TMEM tile.
@@ -46,11 +47,8 @@ struct ScanParams {
     int n_it, total_items;
     int band;    // (sequence, head) pairs per band of the item order
     int stages;  // K stages in the ring
-    unsigned* keys;
-    unsigned* done;  // zeroed counter of finished CTAs
     float sqrt_d;
-    int accumulate;
-    float* s_max;
+    float* s_max;  // filled with 0xFFFFFFFF, or holding the maxima to merge into
     float* s_bh;
     unsigned* status;
 };
@@ -64,7 +62,6 @@ struct ScanSmemTail {
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
-    int last_cta;
 };
 
 
@@ -301,7 +298,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(const __grid_cons
             }
             if (!ok) break;
             float m = warp_max_nan(max_nan(max_nan(m0, m1), max_nan(m2, m3)));
-            if (lane == 0 && m != -INFINITY) atomicMax(&P.keys[b * P.H + h], float_key(m));
+            if (lane == 0 && m != -INFINITY)  // -inf: every row of this warp is past T
+                merge_smax(m, P.sqrt_d, P.s_max, P.s_bh, b, P.H, h, P.status);
         }
     }
 
@@ -310,20 +308,6 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(const __grid_cons
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, 512);
-
-    // the last CTA to finish turns the keys into S_max (threadfence pattern:
-    // every CTA's atomics are visible before its count is)
-    if (threadIdx.x == 0) {
-        __threadfence();
-        const unsigned old = atomicAdd(P.done, 1u);
-        tail->last_cta = old == gridDim.x - 1;
-    }
-    __syncthreads();
-    if (tail->last_cta) {
-        __threadfence();
-        for (int h = threadIdx.x; h < P.H; h += blockDim.x)
-            finalize_head(P.keys, P.B, P.H, h, P.sqrt_d, P.accumulate, P.s_max, P.s_bh, P.status);
-    }
 }
 
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream) {
@@ -353,10 +337,7 @@ cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream) {
     P.kr_col = a.kr_col;
     P.n_it = (a.T + kBM - 1) / kBM;
     P.total_items = a.B * a.H * P.n_it;
-    P.keys = a.keys;
-    P.done = a.keys + (size_t)a.B * a.H;
     P.sqrt_d = sqrtf(a.d);
-    P.accumulate = a.accumulate;
     P.s_max = a.s_max;
     P.s_bh = a.s_bh;
     P.status = device_status_ptr();

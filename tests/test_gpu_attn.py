@@ -84,3 +84,21 @@ def test_attention_accumulate_and_max_logit_semantics():
     _, r2 = oracle.attention_mha_np(q2, k2, v2, 2, 64)
     ref = np.maximum(r1.max(0), r2.max(0))
     assert np.all(np.abs(s2.cpu().numpy() - ref) / np.abs(ref) < 1e-4)
+
+
+def test_attention_negative_max_logit():
+    """Every logit of a head below zero (its keys are the negated queries,
+    all rows parallel): S_max is negative and goes through the sign-bit
+    path of the merge; a second head with k = q stays positive."""
+    g = torch.Generator().manual_seed(1500)
+    B, T, H, dh = 2, 200, 2, 64
+    u = torch.randn(H * dh, generator=g)
+    a = torch.rand(B, T, 1, generator=g) + 0.5
+    q = (a * u).to(torch.bfloat16)
+    k = q.clone()
+    k[:, :, :dh] = -q[:, :, :dh]
+    v = torch.randn(B, T, H * dh, generator=g).to(torch.bfloat16)
+    for causal in (False, True):
+        _, s = _check(q, k, v, H, dh, causal)
+        s = s.cpu().numpy()
+        assert s[0] < 0 < s[1]

@@ -86,3 +86,30 @@ def test_nonfinite_input_sets_status_and_gamma_one():
     g = api.mc_qk_clip_mha(wq, inp["wk"].to(dev()), 2, 64, torch.tensor(s, device=dev()), 100.0)
     assert torch.equal(g.cpu(), torch.ones(2))
     assert torch.equal(wq, before)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_negative_and_positive_maxima_merge(causal):
+    """The per-item maxima are merged into S_max with integer atomics whose
+    order depends on the sign bit.  Activations that are positive multiples
+    of one vector make every row's projections parallel: with W_k = -W_q a
+    head's logits are all negative, with W_k = W_q all positive.  Head 0 is
+    negative and head 1 positive; S_max and the per-sequence maxima must
+    match the oracle, and accumulating keeps the larger of old and new."""
+    rng = np.random.default_rng(91)
+    B, T, D, H, dh = 2, 300, 128, 2, 64
+    vdir = rng.standard_normal(D)
+    a = rng.uniform(0.5, 1.5, size=(B, T, 1))
+    x = torch.tensor(a * vdir[None, None, :], dtype=torch.float32).to(torch.bfloat16)
+    wq = torch.tensor(rng.standard_normal((D, H * dh)) * 0.1, dtype=torch.float32).to(torch.bfloat16)
+    wk = wq.clone()
+    wk[:, :dh] = -wq[:, :dh]
+    s, s_bh = _run_mha(x, wq, wk, H, dh, causal)
+    ref = oracle.max_logits_mha(x, wq, wk, H, dh, causal)
+    assert (ref[:, 0] < 0).all() and (ref[:, 1] > 0).all()
+    assert rel_err(s_bh, ref).max() < SMAX_RTOL
+    assert np.array_equal(s, s_bh.max(0))
+    # accumulate: an old S_max below the new one on head 0, above it on head 1
+    old = torch.tensor([2.0 * s[0], 2.0 * s[1]], dtype=torch.float32, device=dev())
+    s2, _ = _run_mha(x, wq, wk, H, dh, causal, accumulate=True, s_max=old)
+    assert s2[0] == s[0] and s2[1] == np.float32(2.0 * s[1])
