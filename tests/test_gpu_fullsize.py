@@ -14,6 +14,10 @@ properties that hold at any size cover the rest.
   long MLA    x [1,32768,7168] causal + heavy rows: the 8 planted heads and
               8 cold ones, the MLA clip bit-exact, Muon on W_kva and W_kb
               against the oracle.
+  attention   the forwards of the three attention workloads ([8,1024,16x64],
+              [2,8192,16x128] causal, MLA [2,8192,64 heads] causal): O of
+              four (sequence, head) pairs element by element and
+              S_max of their heads.
 """
 import gc
 
@@ -194,3 +198,70 @@ def test_long_mla_fullsize():
     assert api.mc_read_device_status(clear=True) == 0
     del inp, d
     _free()
+
+
+def _attn_check(o_dev, v_cols, s_max_h, o_ref, s_ref_b):
+    """o_dev [T, d] of one (sequence, head) against the oracle's o_ref
+    [T, d] (bounds of the attention tests: P and O each rounded once to
+    bf16); s_max_h against the max of the oracle's per-sequence maxima."""
+    got = o_dev.double().numpy()
+    vmax = np.abs(v_cols.double().numpy()).max()
+    tol = 2.0 ** -8 * vmax + 2.0 ** -8 * np.abs(o_ref)
+    bad = np.abs(got - o_ref) > tol
+    assert not bad.any(), f"{int(bad.sum())} of {bad.size} outputs off; max err {np.abs(got - o_ref).max()}"
+    ref = max(s_ref_b)
+    assert abs(s_max_h - ref) / abs(ref) < 1e-4, (s_max_h, ref)
+
+
+@pytest.mark.parametrize("name,picks", [
+    ("attn", [(0, 0), (7, 15), (3, 8), (5, 3)]),   # [8, 1024, 16 x 64] non-causal
+    ("attnl", [(1, 5), (0, 12), (0, 0), (1, 15)]),  # [2, 8192, 16 x 128] causal
+])
+def test_attention_mha_fullsize(name, picks):
+    """The attention forward of the bench's MHA workloads in the bench's
+    launch: O of the picked (sequence, head) pairs element by element and
+    S_max of their heads (every sequence of the head) against the oracle."""
+    lib()
+    import bench
+    from muonclip_mc_max_gb300 import api
+    wl = bench.AttnLayer(name)
+    s = wl.make(dev())
+    wl.step_part(s, api, "scan")
+    torch.cuda.synchronize()
+    assert api.mc_read_device_status(clear=True) == 0
+    H, dh, B = wl.H, wl.dh, wl.B
+    q, k, v = s["q"].cpu(), s["k"].cpu(), s["v"].cpu()
+    o, s_max = s["o"].cpu(), s["s_max"].cpu().numpy()
+    del s
+    _free()
+    for b, h in picks:
+        cols = slice(h * dh, (h + 1) * dh)
+        hq, hk, hv = (t[:, :, cols].contiguous() for t in (q, k, v))
+        o_ref, s_ref = oracle.attention_mha_np(hq, hk, hv, 1, dh, wl.causal, batches=range(B), heads=[0])
+        _attn_check(o[b, :, cols], hv[b], s_max[h], o_ref[b, :, 0], s_ref[:, 0])
+
+
+def test_attention_mla_fullsize():
+    """The K2-shaped MLA attention forward of the bench ([2, 8192], 64 heads,
+    causal) in the bench's launch: O of four (sequence, head) pairs and S_max
+    of their heads against the oracle."""
+    lib()
+    import bench
+    from muonclip_mc_max_gb300 import api
+    wl = bench.AttnMlaLayer()
+    s = wl.make(dev())
+    wl.step_part(s, api, "scan")
+    torch.cuda.synchronize()
+    assert api.mc_read_device_status(clear=True) == 0
+    H, B = wl.H, wl.B
+    q, kc, kr, v = s["q"].cpu(), s["k_c"].cpu(), s["k_r"].cpu(), s["v"].cpu()
+    o, s_max = s["o"].cpu(), s["s_max"].cpu().numpy()
+    del s
+    _free()
+    for b, h in [(0, 37), (1, 2), (0, 0), (1, 63)]:
+        hq = q[:, :, h * 192:(h + 1) * 192].contiguous()
+        hkc = kc[:, :, h * 128:(h + 1) * 128].contiguous()
+        hv = v[:, :, h * 128:(h + 1) * 128].contiguous()
+        o_ref, s_ref = oracle.attention_mla_np(hq, hkc, kr, hv, 1, 128, 64, 128, True, batches=range(B),
+                                               heads=[0])
+        _attn_check(o[b, :, h * 128:(h + 1) * 128], hv[b], s_max[h], o_ref[b, :, 0], s_ref[:, 0])
