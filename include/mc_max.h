@@ -103,8 +103,9 @@ size_t mc_max_logits_mha_workspace_size(int B, int T, int D, int H, int dh, mc_d
  * S_max bound; |values| above 65504 set MC_DEV_RANGE); QK^T runs on fp16
  * operands with fp32 accumulation.  Anything else runs a CUDA-core fp32
  * kernel meant for small shapes.
- * Errors: MC_ERR_INVALID_ARG for non-positive sizes or null pointers,
- * MC_ERR_WORKSPACE for a short workspace.
+ * Errors: MC_ERR_INVALID_ARG for non-positive sizes, null pointers or
+ * s_max / s_max_bh not 4-byte aligned, MC_ERR_WORKSPACE for a short
+ * workspace.
  */
 mc_status mc_max_logits_mha(const void* x, const void* wq, const void* wk, mc_dtype dtype,
                             int B, int T, int D, int H, int dh, int causal, int accumulate,
@@ -193,7 +194,8 @@ mc_status mc_max_logits_mla(const mc_mla_layer* layer, const void* x, int B, int
  *   o         device bf16 [B][T][H*dh], written (must not alias q, k, v)
  *   s_max     device f32 [H]; accumulate != 0 max-merges into its contents
  *   s_max_bh  optional device f32 [B][H] (per-sequence maxima), or NULL
- * dh must be 64 or 128; pointers 16-byte aligned; T >= 1.  Tensor cores
+ * dh must be 64 or 128; q, k, v, o 16-byte aligned, s_max / s_max_bh 4-byte
+ * aligned; T >= 1.  Tensor cores
  * compute q.k and P.v with fp32 accumulation; the softmax weights P are
  * rounded once to bf16 for P.v.  NaN logits make s_max NaN and set
  * MC_DEV_NONFINITE.  s_max / s_max_bh are merged into by the forward kernel

@@ -381,6 +381,7 @@ mc_status mc_attention_mha(const void* q, const void* k, const void* v, int B, i
                            mc_stream_t stream_) {
     cudaStream_t stream = (cudaStream_t)stream_;
     if (!q || !k || !v || !o || !s_max) return MC_ERR_INVALID_ARG;
+    if (!aligned4(s_max) || !aligned4(s_max_bh)) return MC_ERR_INVALID_ARG;  // merged into with 32-bit atomics
     if (B <= 0 || T <= 0 || H <= 0 || dh <= 0) return MC_ERR_INVALID_ARG;
     if (dh != 64 && dh != 128) return MC_ERR_UNSUPPORTED;
     if ((int64_t)B * T > INT32_MAX || (int64_t)H * dh > INT32_MAX) return MC_ERR_UNSUPPORTED;
@@ -411,6 +412,7 @@ mc_status mc_attention_mla(const void* q, const void* k_c, const void* k_r, int 
                            float* s_max, float* s_max_bh, void* ws, size_t ws_bytes, mc_stream_t stream_) {
     cudaStream_t stream = (cudaStream_t)stream_;
     if (!q || !k_c || !k_r || !v || !o || !s_max) return MC_ERR_INVALID_ARG;
+    if (!aligned4(s_max) || !aligned4(s_max_bh)) return MC_ERR_INVALID_ARG;  // merged into with 32-bit atomics
     if (B <= 0 || T <= 0 || H <= 0 || nope <= 0 || rope <= 0 || dv <= 0) return MC_ERR_INVALID_ARG;
     if (nope != 128 || rope != 64 || dv != 128) return MC_ERR_UNSUPPORTED;
     if ((int64_t)B * T > INT32_MAX || (int64_t)H * 192 > INT32_MAX) return MC_ERR_UNSUPPORTED;
@@ -454,6 +456,7 @@ mc_status mc_max_logits_mha(const void* x, const void* wq, const void* wk, mc_dt
                             size_t ws_bytes, mc_stream_t stream_) {
     cudaStream_t stream = (cudaStream_t)stream_;
     if (!x || !wq || !wk || !s_max) return MC_ERR_INVALID_ARG;
+    if (!aligned4(s_max) || !aligned4(s_max_bh)) return MC_ERR_INVALID_ARG;  // merged into with 32-bit atomics
     if (B <= 0 || T <= 0 || D <= 0 || H <= 0 || dh <= 0) return MC_ERR_INVALID_ARG;
     if (dtype != MC_F32 && dtype != MC_BF16) return MC_ERR_INVALID_ARG;
     if ((int64_t)B * T > INT32_MAX || (int64_t)H * dh > INT32_MAX) return MC_ERR_UNSUPPORTED;
@@ -584,6 +587,7 @@ mc_status mc_max_logits_mla(const mc_mla_layer* L, const void* x, int B, int T, 
     mc_status st = mla_check(L, true);
     if (st != MC_OK) return st;
     if (!x || !s_max || B <= 0 || T <= 0) return MC_ERR_INVALID_ARG;
+    if (!aligned4(s_max) || !aligned4(s_max_bh)) return MC_ERR_INVALID_ARG;  // merged into with 32-bit atomics
     if ((int64_t)B * T > INT32_MAX) return MC_ERR_UNSUPPORTED;
     if (!aligned16(x) || !aligned16(L->w_qa) || !aligned16(L->w_qb) || !aligned16(L->w_kva) || !aligned16(L->w_kb))
         return MC_ERR_INVALID_ARG;

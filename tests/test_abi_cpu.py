@@ -49,6 +49,11 @@ def test_invalid_arguments_rejected_on_host(lib):
     # bad dtype
     assert lib.mc_max_logits_mha(fake, fake, fake, 7, 2, 8, 64, 1, 64, 0, 0, fake, nil, ws,
                                  1 << 30, nil) == 1
+    # S_max outputs not 4-byte aligned (the kernels merge into them with 32-bit atomics)
+    assert lib.mc_max_logits_mha(fake, fake, fake, 1, 2, 8, 64, 1, 64, 0, 0, ctypes.c_void_p(4098), nil,
+                                 ws, 1 << 30, nil) == 1
+    assert lib.mc_max_logits_mha(fake, fake, fake, 1, 2, 8, 64, 1, 64, 0, 0, fake, ctypes.c_void_p(4098),
+                                 ws, 1 << 30, nil) == 1
     # Muon: a zero-size matrix, a pointer that is not float-aligned, an empty batch
     rows = (ctypes.c_int * 1)(8)
     cols = (ctypes.c_int * 1)(0)
@@ -78,6 +83,7 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert lib.mc_attention_mha(ctypes.c_void_p(4104), k, v, 1, 8, 2, 64, 0, 0, o, fake, nil, ws, big,
                                 nil) == 1
     assert lib.mc_attention_mha(q, k, v, 1, 8, 2, 64, 0, 0, q, fake, nil, ws, big, nil) == 1
+    assert lib.mc_attention_mha(q, k, v, 1, 8, 2, 64, 0, 0, o, ctypes.c_void_p(4098), nil, ws, big, nil) == 1
     # bounded-wait self-test: limit out of range, null or misaligned result
     assert lib.mc_selftest_wait_timeout(0, fake, nil) == 1
     assert lib.mc_selftest_wait_timeout(1000001, fake, nil) == 1
