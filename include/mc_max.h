@@ -244,6 +244,9 @@ mc_status mc_attention_mla(const void* q, const void* k_c, const void* k_r, int 
  * storage type (bf16 or f32).  Heads with gamma_h == 1 are not written, so
  * their bits are unchanged.  gamma [H] f32 out, may be NULL.
  * Apply after the optimizer update, with this step's S_max.
+ * Errors (all clips): MC_ERR_INVALID_ARG for null or non-positive
+ * arguments, a weight pointer not aligned to its element (2 bytes bf16,
+ * 4 bytes f32), or s_max / gamma not 4-byte aligned.
  */
 mc_status mc_qk_clip_mha(void* wq, void* wk, mc_dtype dtype, int D, int H, int dh,
                          const float* s_max, float tau, float* gamma, mc_stream_t stream);

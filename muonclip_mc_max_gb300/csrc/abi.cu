@@ -221,6 +221,10 @@ struct Carve {
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 static bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; }
+// a weight pointer aligned to its element (2 bytes for bf16, 4 for f32)
+static bool aligned_elem(const void* p, mc_dtype dt) {
+    return (reinterpret_cast<uintptr_t>(p) & (dt == MC_BF16 ? 1u : 3u)) == 0;
+}
 
 // Projection D = A W with W [K][N] row-major (the MN-major B operand);
 // A and W both bf16 (f16 = 0) or both fp16 (f16 = 1); D stored in fp16.
@@ -666,6 +670,8 @@ mc_status mc_qk_clip_mha(void* wq, void* wk, mc_dtype dtype, int D, int H, int d
                          float* gamma, mc_stream_t stream) {
     if (!wq || !wk || !s_max || D <= 0 || H <= 0 || dh <= 0) return MC_ERR_INVALID_ARG;
     if (dtype != MC_F32 && dtype != MC_BF16) return MC_ERR_INVALID_ARG;
+    if (!aligned_elem(wq, dtype) || !aligned_elem(wk, dtype) || !aligned4(s_max) || !aligned4(gamma))
+        return MC_ERR_INVALID_ARG;
     ClipArgs a;
     memset(&a, 0, sizeof(a));
     a.nseg = 2;
@@ -691,6 +697,9 @@ mc_status mc_qk_clip_mla(const mc_mla_layer* L, const float* s_max, float tau, f
     mc_status st = mla_check(L, false);
     if (st != MC_OK) return st;
     if (!s_max) return MC_ERR_INVALID_ARG;
+    if (!aligned_elem(L->w_qb, (mc_dtype)L->wtype) || !aligned_elem(L->w_kb, (mc_dtype)L->wtype) || !aligned4(s_max) ||
+        !aligned4(gamma))
+        return MC_ERR_INVALID_ARG;
     const int qk = L->nope + L->rope;
     ClipArgs a;
     memset(&a, 0, sizeof(a));
@@ -719,6 +728,8 @@ mc_status mc_qk_clip_global(void* wq, void* wk, mc_dtype dtype, int rows, int co
                             float tau, float alpha, float* gamma_out, mc_stream_t stream) {
     if (!wq || !wk || !s_max || rows <= 0 || cols <= 0 || H <= 0) return MC_ERR_INVALID_ARG;
     if (dtype != MC_F32 && dtype != MC_BF16) return MC_ERR_INVALID_ARG;
+    if (!aligned_elem(wq, dtype) || !aligned_elem(wk, dtype) || !aligned4(s_max) || !aligned4(gamma_out))
+        return MC_ERR_INVALID_ARG;
     MC_CUDA(launch_clip_global(wq, wk, dtype == MC_BF16, (long long)rows * cols, s_max, H, tau, alpha, gamma_out,
                                (cudaStream_t)stream));
     return MC_OK;

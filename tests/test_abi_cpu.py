@@ -84,6 +84,15 @@ def test_invalid_arguments_rejected_on_host(lib):
                                 nil) == 1
     assert lib.mc_attention_mha(q, k, v, 1, 8, 2, 64, 0, 0, q, fake, nil, ws, big, nil) == 1
     assert lib.mc_attention_mha(q, k, v, 1, 8, 2, 64, 0, 0, o, ctypes.c_void_p(4098), nil, ws, big, nil) == 1
+    # QK-Clip: a bf16 weight at an odd address, an f32 weight or S_max not 4-byte aligned
+    assert lib.mc_qk_clip_mha(ctypes.c_void_p(4097), fake, 1, 8, 2, 64, fake, ctypes.c_float(100.0), nil,
+                              nil) == 1
+    assert lib.mc_qk_clip_mha(ctypes.c_void_p(4098), fake, 0, 8, 2, 64, fake, ctypes.c_float(100.0), nil,
+                              nil) == 1
+    assert lib.mc_qk_clip_mha(fake, fake, 1, 8, 2, 64, ctypes.c_void_p(4098), ctypes.c_float(100.0), nil,
+                              nil) == 1
+    assert lib.mc_qk_clip_global(ctypes.c_void_p(4097), fake, 1, 8, 8, fake, 2, ctypes.c_float(100.0),
+                                 ctypes.c_float(0.5), nil, nil) == 1
     # bounded-wait self-test: limit out of range, null or misaligned result
     assert lib.mc_selftest_wait_timeout(0, fake, nil) == 1
     assert lib.mc_selftest_wait_timeout(1000001, fake, nil) == 1
