@@ -463,6 +463,7 @@ mc_status mc_max_logits_mha(const void* x, const void* wq, const void* wk, mc_dt
     if (!aligned4(s_max) || !aligned4(s_max_bh)) return MC_ERR_INVALID_ARG;  // merged into with 32-bit atomics
     if (B <= 0 || T <= 0 || D <= 0 || H <= 0 || dh <= 0) return MC_ERR_INVALID_ARG;
     if (dtype != MC_F32 && dtype != MC_BF16) return MC_ERR_INVALID_ARG;
+    if (!aligned_elem(x, dtype) || !aligned_elem(wq, dtype) || !aligned_elem(wk, dtype)) return MC_ERR_INVALID_ARG;
     if ((int64_t)B * T > INT32_MAX || (int64_t)H * dh > INT32_MAX) return MC_ERR_UNSUPPORTED;
     size_t need = mc_max_logits_mha_workspace_size(B, T, D, H, dh, dtype);
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < need) return MC_ERR_WORKSPACE;
