@@ -103,7 +103,8 @@ size_t mc_max_logits_mha_workspace_size(int B, int T, int D, int H, int dh, mc_d
  * S_max bound; |values| above 65504 set MC_DEV_RANGE); QK^T runs on fp16
  * operands with fp32 accumulation.  Anything else runs a CUDA-core fp32
  * kernel meant for small shapes.
- * Errors: MC_ERR_INVALID_ARG for non-positive sizes, null pointers or
+ * Errors: MC_ERR_INVALID_ARG for non-positive sizes, null pointers, x / wq /
+ * wk not aligned to their element (16 bytes on the tensor-core path) or
  * s_max / s_max_bh not 4-byte aligned, MC_ERR_WORKSPACE for a short
  * workspace.
  */
