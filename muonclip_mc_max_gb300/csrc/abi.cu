@@ -866,6 +866,7 @@ mc_status run_mat_pass(const NsPlan& P, int mode, float* const* w, const float* 
             d.vec = cols[i] % 4 == 0 &&
                     (mode == 0 ? aligned16(m[i]) && aligned16(g[i])
                                : mode == 1 ? aligned16(in[i]) : aligned16(w[i]));
+            d.flat = d.vec && !d.tr && gr.m_pad == rows[i] && gr.n_pad == cols[i];
             if (mode == 0) {
                 d.m = m[i];
                 d.g = g[i];

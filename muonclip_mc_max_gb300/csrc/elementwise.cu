@@ -231,7 +231,75 @@ __global__ void __launch_bounds__(kMatThreads) mat_pass_kernel(const __grid_cons
         const int m = d.tr ? d.cols : d.rows, n = d.tr ? d.rows : d.cols;
         const bool any = i0 < m && j0 < n;
 
-        if (B.mode <= 1) {
+        // flat matrices: X has the source's own layout (no transpose, no
+        // padding), so chunk `local` is 4096 consecutive elements of both and
+        // each warp streams whole 512-byte runs; the chunks take the places of
+        // the tiles (one sum of squares each)
+        const size_t fbase = (size_t)local * (kTile * kTile) + tid * 4;
+
+        if (B.mode <= 1 && d.flat) {
+            float ss = 0.f;
+#pragma unroll 1
+            for (int p = 0; p < 4; ++p) {
+                const size_t off = fbase + (size_t)p * (kMatThreads * 4);
+                float4 u = *reinterpret_cast<const float4*>(d.m + off);
+                if (B.mode == 0) {
+                    const float4 gv = *reinterpret_cast<const float4*>(d.g + off);
+                    float4 mv;
+                    mv.x = __fmaf_rn(B.mu, u.x, gv.x);
+                    mv.y = __fmaf_rn(B.mu, u.y, gv.y);
+                    mv.z = __fmaf_rn(B.mu, u.z, gv.z);
+                    mv.w = __fmaf_rn(B.mu, u.w, gv.w);
+                    *reinterpret_cast<float4*>(d.m + off) = mv;
+                    u = B.nesterov ? make_float4(__fmaf_rn(B.mu, mv.x, gv.x), __fmaf_rn(B.mu, mv.y, gv.y),
+                                                 __fmaf_rn(B.mu, mv.z, gv.z), __fmaf_rn(B.mu, mv.w, gv.w))
+                                   : mv;
+                }
+                ss += u.x * u.x + u.y * u.y + u.z * u.z + u.w * u.w;
+                __nv_bfloat162 h0 = __floats2bfloat162_rn(u.x, u.y);
+                __nv_bfloat162 h1 = __floats2bfloat162_rn(u.z, u.w);
+                uint2 pk;
+                pk.x = *reinterpret_cast<uint32_t*>(&h0);
+                pk.y = *reinterpret_cast<uint32_t*>(&h1);
+                *reinterpret_cast<uint2*>(d.x + off) = pk;
+            }
+            double s = (double)ss;
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+            if ((tid & 31) == 0) red[tid >> 5] = s;
+            __syncthreads();
+            if (tid == 0) {
+                double tot = 0.0;
+                for (int w = 0; w < kMatThreads / 32; ++w) tot += red[w];
+                d.partial[local] = tot;
+            }
+            __syncthreads();
+        } else if (d.flat) {
+            const float osc = d.oscale ? *d.oscale : 1.0f;
+#pragma unroll 1
+            for (int p = 0; p < 4; ++p) {
+                const size_t off = fbase + (size_t)p * (kMatThreads * 4);
+                uint2 pk = *reinterpret_cast<const uint2*>(d.x + off);
+                float2 a, b;
+                if (B.x_f16) {
+                    a = __half22float2(*reinterpret_cast<__half2*>(&pk.x));
+                    b = __half22float2(*reinterpret_cast<__half2*>(&pk.y));
+                } else {
+                    a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&pk.x));
+                    b = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&pk.y));
+                }
+                const float o0 = osc * a.x, o1 = osc * a.y, o2 = osc * b.x, o3 = osc * b.y;
+                if (B.mode == 2) {
+                    float4 w = *reinterpret_cast<const float4*>(d.w + off);
+                    w.x = muon_update_elem(w.x, o0, B.lr, d.rms, B.wd);
+                    w.y = muon_update_elem(w.y, o1, B.lr, d.rms, B.wd);
+                    w.z = muon_update_elem(w.z, o2, B.lr, d.rms, B.wd);
+                    w.w = muon_update_elem(w.w, o3, B.lr, d.rms, B.wd);
+                    *reinterpret_cast<float4*>(d.w + off) = w;
+                } else {
+                    *reinterpret_cast<float4*>(d.w + off) = make_float4(o0, o1, o2, o3);
+                }
+            }
+        } else if (B.mode <= 1) {
             // ---- momentum (+ Nesterov) and cast: source -> U -> X ----
             float ss = 0.f;
             if (any) {

@@ -235,6 +235,7 @@ struct MatDesc {
     float rms;           // mode 2: rms_coef * sqrt(max(rows, cols))
     int rows, cols, tr;  // tr: X = transpose of the matrix (rows > cols)
     int vec;             // cols % 4 == 0 and 16-byte aligned rows: float4 accesses
+    int flat;            // X has the source's layout (vec, no transpose, no padding): 4096-element chunks
     int m_pad, n_pad;
     int tiles_x, tile_begin;  // 64 x 64 tiles over X [m_pad][n_pad]
 };
