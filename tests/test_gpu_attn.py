@@ -54,6 +54,10 @@ def _check(q, k, v, H, dh, causal):
     (2, 77, 2, 128),    # dh = 128 below one tile
     (2, 200, 2, 128),   # dh = 128, two query tiles, ragged key tail
     (1, 1030, 1, 128),  # dh = 128, nine key blocks through its two K stages
+    (3, 1, 2, 64),      # a single token
+    (2, 1, 1, 128),     # a single token, dh = 128
+    (1, 129, 2, 64),    # one row past the first tile
+    (1, 257, 1, 128),   # one row past a pair of tiles, dh = 128
 ])
 def test_attention_vs_oracle(shape, causal):
     B, T, H, dh = shape

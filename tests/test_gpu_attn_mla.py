@@ -55,6 +55,9 @@ def _check(inp, causal, kr_in_latent=False):
     (2, 128, 1),    # exactly one tile
     (2, 77, 3),     # T below one tile
     (1, 1030, 1),   # nine key blocks, tail of 6
+    (3, 1, 2),      # a single token
+    (1, 129, 2),    # one row past the first tile
+    (1, 256, 1),    # exactly one pair of tiles
 ])
 def test_attention_mla_vs_oracle(shape, causal):
     B, T, H = shape

@@ -30,6 +30,7 @@ def _mla(inp, causal):
 @pytest.mark.parametrize("dims", [
     dict(B=2, T=200, D=256, H=2, q_lora=128, kv_lora=64),
     dict(B=1, T=520, D=128, H=3, q_lora=192, kv_lora=128),
+    dict(B=1, T=257, D=128, H=2, q_lora=128, kv_lora=64),   # one key past a 256-key tile
 ])
 def test_mla_scan_vs_oracle(dims, causal):
     inp = mc_inputs.mla_layer(**dims, n_hot=1, w_std=0.05, seed=31 + dims["T"], causal=causal)

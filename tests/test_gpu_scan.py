@@ -38,6 +38,7 @@ def test_c1_fp32_page_example():
     (1, 128, 64, 1, 64),     # exactly one query tile
     (3, 77, 128, 2, 128),    # dh = 128: two K blocks per head, T < one tile
     (1, 1030, 256, 2, 64),   # many tiles, ragged tail of 6
+    (1, 257, 128, 1, 64),    # one key past a 256-key tile, one row past two query tiles
 ])
 def test_mha_bf16_tensor_path(shape, causal):
     B, T, D, H, dh = shape
