@@ -204,6 +204,22 @@ MC_D void find_mat(const MatBatch& B, int t, int& di) {
     while (di + 1 < B.count && t >= B.d[di + 1].tile_begin) ++di;
 }
 
+// The CTA's sum of the threads' partial sums of squares, in fp64 and in a
+// fixed order (lanes by butterfly, then warps in turn), stored at *out.
+MC_D void block_sumsq(float ss, double* red, double* out) {
+    const int tid = threadIdx.x;
+    double s = (double)ss;
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+    if ((tid & 31) == 0) red[tid >> 5] = s;
+    __syncthreads();
+    if (tid == 0) {
+        double tot = 0.0;
+        for (int w = 0; w < kMatThreads / 32; ++w) tot += red[w];
+        *out = tot;
+    }
+    __syncthreads();
+}
+
 // Source element (r, c) of the [rows][cols] matrix <-> X element (i, j):
 // X = S^T when tr, else X = S.
 __global__ void __launch_bounds__(kMatThreads) mat_pass_kernel(const __grid_constant__ MatBatch B) {
@@ -263,16 +279,7 @@ __global__ void __launch_bounds__(kMatThreads) mat_pass_kernel(const __grid_cons
                 pk.y = *reinterpret_cast<uint32_t*>(&h1);
                 *reinterpret_cast<uint2*>(d.x + off) = pk;
             }
-            double s = (double)ss;
-            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
-            if ((tid & 31) == 0) red[tid >> 5] = s;
-            __syncthreads();
-            if (tid == 0) {
-                double tot = 0.0;
-                for (int w = 0; w < kMatThreads / 32; ++w) tot += red[w];
-                d.partial[local] = tot;
-            }
-            __syncthreads();
+            block_sumsq(ss, red, d.partial + local);
         } else if (d.flat) {
             const float osc = d.oscale ? *d.oscale : 1.0f;
 #pragma unroll 1
@@ -370,17 +377,7 @@ __global__ void __launch_bounds__(kMatThreads) mat_pass_kernel(const __grid_cons
                 pk.y = *reinterpret_cast<uint32_t*>(&h1);
                 *reinterpret_cast<uint2*>(d.x + (size_t)(i0 + li) * d.n_pad + j0 + lj) = pk;
             }
-            // deterministic tile sum of squares
-            double s = (double)ss;
-            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
-            if ((tid & 31) == 0) red[tid >> 5] = s;
-            __syncthreads();
-            if (tid == 0) {
-                double tot = 0.0;
-                for (int w = 0; w < kMatThreads / 32; ++w) tot += red[w];
-                d.partial[local] = tot;
-            }
-            __syncthreads();
+            block_sumsq(ss, red, d.partial + local);  // deterministic tile sum of squares
         } else {
             // ---- X -> U -> update W (mode 2) or write O (mode 3) ----
             if (!any) continue;
