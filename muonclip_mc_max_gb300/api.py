@@ -226,7 +226,8 @@ def mc_attention_mha_workspace_size(B: int, H: int) -> int:
 def mc_attention_mha(q, k, v, H: int, dh: int, causal: bool = False, accumulate: bool = False,
                      out=None, s_max=None, s_max_bh=None, workspace=None, stream=None):
     """q, k, v [B,T,H*dh] bf16.  Returns (o [B,T,H*dh] bf16, s_max [H] f32):
-    softmax attention with the per-head max logit taken along."""
+    softmax attention with the per-head max logit taken along.  The forward
+    needs no workspace (``workspace`` is accepted and not used)."""
     lib = load_library()
     _need_cuda(q, k, v, out, s_max, s_max_bh)
     B, T, W = q.shape
