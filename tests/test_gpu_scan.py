@@ -66,10 +66,12 @@ def test_accumulate_is_max_over_microbatches():
     wq, wk = a["wq"], a["wk"]
     s1, _ = _run_mha(a["x"], wq, wk, 2, 64, True)
     s_dev = torch.tensor(s1, device=dev())
-    s2, _ = _run_mha(b["x"], wq, wk, 2, 64, True, accumulate=True, s_max=s_dev)
-    ref = np.maximum(oracle.max_logits_mha(a["x"], wq, wk, 2, 64, True).max(0),
-                     oracle.max_logits_mha(b["x"], wq, wk, 2, 64, True).max(0))
+    s2, s_bh2 = _run_mha(b["x"], wq, wk, 2, 64, True, accumulate=True, s_max=s_dev)
+    ref_b = oracle.max_logits_mha(b["x"], wq, wk, 2, 64, True)
+    ref = np.maximum(oracle.max_logits_mha(a["x"], wq, wk, 2, 64, True).max(0), ref_b.max(0))
     assert rel_err(s2, ref).max() < SMAX_RTOL
+    # the per-sequence maxima are this call's alone (only s_max accumulates)
+    assert rel_err(s_bh2, ref_b).max() < SMAX_RTOL
 
 
 def test_nonfinite_input_sets_status_and_gamma_one():
